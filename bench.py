@@ -1,0 +1,489 @@
+"""Benchmark of the paged KV hot path on GB300: one step = for every layer,
+append the step's token(s) per row with fused quantization, then paged GQA
+decode attention (split-K + LSE merge) through the block tables.
+
+Default workload (N = 1): INT8-G64 compact decode batch, C = 8 rows with
+contexts uniform in [1, 4096] after the append, 16 q / 2 kv heads, head_dim
+256, 8 layers, pool of M = 512 shuffled pages.  Other workloads: --workload.
+
+Prints ONE JSON line (rank 0).  `value` is KV GB/s of the whole step:
+algorithmic bytes (each valid KV token-head read once, shared pages once,
+plus q / out / lse / appended K,V and codes) over the device time of the
+step, inputs resident in HBM, L2 flushed before every timed step.  `e2e` is
+the same metric through the C ABI with the step's inputs copied from pinned
+host memory and the outputs copied back inside the timed region.
+
+--impl reference times the oracle (plain NumPy float64, test
+infrastructure) on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and decode rows/s at C=1..8"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def make_workload(name):
+    from paged_kv_cache_append_gb300 import workloads as W
+    if name == "k8v4_verify":
+        return W.k8v4_long(T=4)
+    return W.WORKLOADS[name]()
+
+
+def workload_desc(w):
+    return (f"{w.name}: {w.profile}, C={w.C} rows, T={w.T}, {w.Hq}q/{w.Hkv}kv heads, D={w.D}, "
+            f"{w.num_layers} layers, S={w.S}, M={w.M}, contexts {int(w.context.min()) + w.T}.."
+            f"{int(w.context.max()) + w.T}")
+
+
+# ------------------------------------------------------------ clock sampler
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+
+class Bench:
+    """Device state of one workload; `share` reuses another Bench's filled
+    pool (a sub-batch of its first B rows)."""
+
+    def __init__(self, w, device, B=None, share=None):
+        import torch
+        from paged_kv_cache_append_gb300 import nk
+        self.torch, self.nk, self.w, self.dev = torch, nk, w, device
+        B = w.B if B is None else B
+        self.B = B
+        self.tables = torch.from_numpy(w.tables).to(device)
+        self.rows = torch.from_numpy(w.table_rows[:B].copy()).to(device)
+        self.ctx = torch.from_numpy(w.context[:B].copy()).to(device)
+        self.front = torch.from_numpy((w.context[:B] + w.T).astype(np.int32)).to(device)
+        if share is not None:
+            self.pool = share.pool
+        else:
+            self.pool = nk.Pool(w.profile, w.num_layers, w.Hkv, w.D, w.S, w.C, w.M, device=device)
+            self._fill()
+        # per-layer step inputs, resident on the device
+        self.q, self.k, self.v = [], [], []
+        for layer in range(w.num_layers):
+            self.q.append(w.step_q(layer)[:B].contiguous().to(device))
+            k, v = w.step_kv(layer)
+            self.k.append(k[:B].contiguous().to(device))
+            self.v.append(v[:B].contiguous().to(device))
+        self.out = [torch.empty_like(x) for x in self.q]
+        self.lse = [torch.empty((B, w.T, w.Hq), dtype=torch.float32, device=device) for _ in self.q]
+        n = nk.nk_decode_workspace_bytes(self.pool.handle, B, w.T, w.Hq)
+        self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+        self.launches_per_step = 3 * w.num_layers    # append + decode + merge per layer
+
+    def _fill(self):
+        """Context of every table row (device-side seeded values), written
+        with the library's append; shared-prefix rows reuse row 0's pages."""
+        torch, w = self.torch, self.w
+        P = 64
+        sh, full, tail = w.shared_len, w.shared_len // P, w.shared_len % P
+        ctx = np.zeros(w.C, np.int64)
+        ctx[w.table_rows] = w.context
+        gen_dev = self.dev if w.S * w.C * w.Hkv * w.D > (1 << 26) else "cpu"
+        for layer in range(w.num_layers):
+            for r in range(w.C):
+                start = sh if (sh and r > 0) else 0
+                n = int(ctx[r]) - start
+                if n <= 0:
+                    continue
+                k, v = w.context_kv(layer, r, int(ctx[r]), device=gen_dev)
+                for t0 in range(start, int(ctx[r]), 32768):
+                    t1 = min(int(ctx[r]), t0 + 32768)
+                    kk = k[t0:t1].unsqueeze(0).contiguous().to(self.dev)
+                    vv = v[t0:t1].unsqueeze(0).contiguous().to(self.dev)
+                    self.pool.append(layer, self.tables,
+                                     torch.tensor([r], dtype=torch.int32, device=self.dev),
+                                     torch.tensor([t0], dtype=torch.int32, device=self.dev), kk, vv)
+                del k, v
+            if sh and tail and layer == w.num_layers - 1:
+                for r in range(1, w.C):
+                    self.pool.copy_columns(int(w.tables[0, full]), int(w.tables[r, full]), tail)
+        torch.cuda.synchronize()
+
+    def step(self, stream=None):
+        w = self.w
+        for layer in range(w.num_layers):
+            self.pool.append(layer, self.tables, self.rows, self.ctx, self.k[layer], self.v[layer],
+                             stream=stream)
+            self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
+                             out=self.out[layer], lse=self.lse[layer], workspace=self.ws, stream=stream)
+
+    def decode_only(self, layer):
+        w = self.w
+        self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
+                         out=self.out[layer], lse=self.lse[layer], workspace=self.ws)
+
+    # -- accounting --------------------------------------------------------
+    def bytes_decode_layer(self):
+        """Algorithmic bytes of one decode launch (one layer): every valid KV
+        token-head once (pages shared by several rows once), plus q, out, lse."""
+        w = self.w
+        bpt = self.pool.kv_bytes_per_token_head()
+        F = (w.context[:self.B] + w.T).astype(np.int64)
+        tokens = int(F.sum())
+        if w.shared_len:
+            tokens -= (self.B - 1) * min(w.shared_len, int(F.min()))
+        kv = tokens * w.Hkv * bpt
+        qo = self.B * w.T * w.Hq * (2 * w.D * 2 + 4)
+        return kv + qo
+
+    def bytes_append_layer(self):
+        w = self.w
+        return self.B * w.T * w.Hkv * (2 * w.D * 2 + self.pool.kv_bytes_per_token_head())
+
+    def bytes_step(self):
+        return self.w.num_layers * (self.bytes_decode_layer() + self.bytes_append_layer())
+
+
+def _flush_fn(torch, device):
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    buf = torch.empty(max(2 * l2, 1 << 28) // 4, dtype=torch.float32, device=device)
+    return lambda: buf.fill_(1.0), 2 * l2
+
+
+def run_gpu(args, rank, world):
+    import torch
+    device = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
+    torch.cuda.set_device(device)
+    w = make_workload(args.workload)
+    hbm_peak, peak_kind = peaks()
+    bench = Bench(w, device)
+    flush, flush_bytes = _flush_fn(torch, device)
+    stream = torch.cuda.current_stream()
+
+    # warm-up (eager), then capture one step in a CUDA graph
+    for _ in range(max(args.warmup, 3)):
+        bench.step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        bench.step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, L2 flushed before each --------------------
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        t_wall = time.perf_counter()
+        for e0, e1 in evs:
+            flush()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    # ---- dominant kernel: one decode launch (decode + merge), per layer ----
+    kev = []
+    for _ in range(max(3, args.steps // 2)):
+        for layer in range(w.num_layers):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush()
+            e0.record(stream)
+            bench.decode_only(layer)
+            e1.record(stream)
+            kev.append((e0, e1))
+    torch.cuda.synchronize()
+    kms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in kev)
+    achieved = bench.bytes_decode_layer() / (kms * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    qh = [x.cpu().pin_memory() for x in bench.q]
+    kh = [x.cpu().pin_memory() for x in bench.k]
+    vh = [x.cpu().pin_memory() for x in bench.v]
+    oh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bench.out]
+    lh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bench.lse]
+    h2d = sum(x.numel() * x.element_size() for x in qh + kh + vh)
+    d2h = sum(x.numel() * x.element_size() for x in oh + lh)
+
+    def e2e_step():
+        for i in range(w.num_layers):
+            bench.q[i].copy_(qh[i], non_blocking=True)
+            bench.k[i].copy_(kh[i], non_blocking=True)
+            bench.v[i].copy_(vh[i], non_blocking=True)
+        graph.replay()
+        for i in range(w.num_layers):
+            oh[i].copy_(bench.out[i], non_blocking=True)
+            lh[i].copy_(bench.lse[i], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    eev = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        eev.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in eev)
+
+    # ---- rows/s at C = 1..8 ------------------------------------------------------
+    sweep = {}
+    if not args.no_sweep and w.B > 1:
+        for c in range(1, w.B + 1):
+            bc = Bench(w, device, B=c, share=bench) if c != w.B else bench
+            g = torch.cuda.CUDAGraph()
+            bc.step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                bc.step()
+            g.replay()
+            torch.cuda.synchronize()
+            tt = []
+            for _ in range(max(5, args.steps // 4)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                tt.append((e0, e1))
+            torch.cuda.synchronize()
+            sm = statistics.mean(a.elapsed_time(b) for a, b in tt)
+            sweep[str(c)] = {"rows_per_s": round(c * w.T / (sm * 1e-3), 1),
+                             "kv_gbs": round(bc.bytes_step() / (sm * 1e-3) / 1e9, 1),
+                             "ms_per_step": round(sm, 4)}
+            del bc
+
+    value = world * bench.bytes_step() / (ms * 1e-3) / 1e9
+    e2e_val = world * bench.bytes_step() / (e2e_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": (f"{w.profile} KV codes; " + ("bf16" if w.profile == "bf16" else "f16")
+                  + " mma, fp32 accumulate"),
+        "data": "synthetic (seeded N(0,1) bf16; tables are seeded permutations)",
+        "config": {"workload": workload_desc(w), "rows": bench.B, "layers": w.num_layers,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": f"flushed ({flush_bytes >> 20} MiB write) before every timed step",
+                   "graph": "one CUDA graph per step"},
+        "rows_per_s": round(bench.B * w.T / (ms * 1e-3), 1),
+        "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": None, "kernel": "nk_paged_decode_attention (decode + merge), one layer",
+                     "algorithmic_bytes_per_launch": bench.bytes_decode_layer(),
+                     "avg_launch_ms": round(kms, 5)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": bench.launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(t_wall, 4),
+    }
+    if sweep:
+        line["sweep_rows_per_s"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------ oracle arm
+
+def oracle_sample(w, rows, layer=0):
+    """One decode step of the oracle for `rows` of one layer: encode the
+    context and the step token, gather through the table, attend.  Returns
+    the algorithmic bytes this covers (same accounting as the GPU arm)."""
+    from oracle import attention as OA, codec as OC, formats as OF
+    from paged_kv_cache_append_gb300.workloads import bf16_to_bits
+    ks, vs = w.step_kv(layer)
+    q = w.step_q(layer)
+    total = 0
+    for b in rows:
+        r = int(w.table_rows[b])
+        n = int(w.context[b])
+        kc, vc = w.context_kv(layer, r, n)
+        kb = np.concatenate([bf16_to_bits(kc), bf16_to_bits(ks[b])], axis=0)
+        vb = np.concatenate([bf16_to_bits(vc), bf16_to_bits(vs[b])], axis=0)
+        planes = OC.encode_kv(w.profile, kb, vb)
+        K, V = OC.decode_kv(w.profile, planes)
+        OA.decode(OF.bf16_bits_to_f64(bf16_to_bits(q[b])), K, V, n + w.T, w.scale)
+        bpt = sum(p.shape[-1] for p in planes.values())
+        total += (n + w.T) * w.Hkv * bpt + w.T * w.Hq * (2 * w.D * 2 + 4)
+    return total
+
+
+def cpu_baseline(w, seconds=15.0):
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    done, rows = 0, []
+    b = 0
+    while time.perf_counter() - t0 < seconds and b < w.B:
+        done += oracle_sample(w, [b])
+        rows.append(b)
+        b += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"layer 0, rows {rows} of {w.name}: encode context + step token, gather, "
+                      f"float64 attention ({dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    w = make_workload(args.workload)
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        oracle_sample(w, [0])
+    times, done = [], 0
+    rows_per_step = 1
+    for s in range(args.steps):
+        t0 = time.perf_counter()
+        done += oracle_sample(w, [s % w.B][:rows_per_step])
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = done / tot / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": workload_desc(w), "sample": "each step: one row, one layer"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: one decode row of layer 0 (encode, gather, attend)"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="nk", choices=["nk", "reference"])
+    ap.add_argument("--workload", default="int8_decode",
+                    choices=["tiny_bf16", "int8_decode", "fp8_shared", "k8v4_long", "k8v4_verify"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

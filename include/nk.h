@@ -1,0 +1,227 @@
+/*
+ * nk.h -- C ABI of libnk: paged KV cache append and paged attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Source of the contract: the "Paged KV cache" maintainer design page of the
+ * NInfer inference engine (typed growing KV pools, P = 64 token pages, block
+ * tables, non-owning consumer views).  Section names below refer to that page
+ * unless another page is named.
+ *
+ * Conventions for every call
+ *  - Every pointer argument marked "device" points to GPU memory owned by the
+ *    caller; libnk never allocates, frees or retains caller memory beyond the
+ *    call (a pool handle borrows its plane pointers for its lifetime).
+ *  - Calls that take a cudaStream_t (passed as void*) are asynchronous on that
+ *    stream, never synchronize, and launch nothing when they return an error.
+ *    NULL means the legacy default stream.
+ *  - Return value: NK_OK (0) or a negative NK_ERR_* code; nk_last_error()
+ *    then describes the failure (thread-local text).  No exception crosses
+ *    the ABI.  Argument checks happen on the host before any launch, so an
+ *    error return has no side effect.
+ *  - Caller guarantees (consumer view section, "wrapper validates / caller
+ *    guarantees"): every logical block a call may touch is mapped in its
+ *    table row, reads stay below the frozen valid frontier, the table rows in
+ *    use are not rewritten while the call is in flight.  The kernels still
+ *    never access memory outside the pool when a guarantee is broken: a page
+ *    id outside [0, M), a table row outside [0, C) or a position / frontier
+ *    outside [0, L*P] is skipped (append) or read as page 0 / an empty row
+ *    (attention), the affected results are undefined, and an NK_STATUS_* bit
+ *    is recorded in the device status word (nk_status_read).
+ *  - bf16 tensors are little-endian IEEE bfloat16; layouts are C order
+ *    (row-major, last index fastest).
+ */
+#ifndef NK_H_
+#define NK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NK_PAGE_TOKENS 64 /* P: allocation granularity of every growing pool */
+
+/* Return codes. */
+enum {
+  NK_OK = 0,
+  NK_ERR_INVALID_ARG = -1, /* null pointer, bad enum, non-finite scale       */
+  NK_ERR_SHAPE = -2,       /* B, T, Hq, head_dim or layer out of range        */
+  NK_ERR_RANGE = -3,       /* page-group count M outside [M_min, M_max]       */
+  NK_ERR_UNSUPPORTED = -4, /* profile / head_dim / GQA combination not built  */
+  NK_ERR_ALIGN = -5,       /* pointer not 16-byte aligned                     */
+  NK_ERR_CUDA = -6,        /* a CUDA runtime or driver call failed            */
+  NK_ERR_WORKSPACE = -7    /* workspace smaller than required                 */
+};
+
+/* Bits of the device status word (nk_status_read). */
+enum {
+  NK_STATUS_PAGE_RANGE = 1,  /* a table entry was outside [0, M)             */
+  NK_STATUS_FRONTIER = 2,    /* a position reached past L*P of its row       */
+  NK_STATUS_TIMEOUT = 4      /* a bounded wait on a copy barrier ran out     */
+};
+
+/* KV profiles ("Paged KV cache" page, pool contents paragraph: BF16,
+ * INT8-G64, FP8-E4M3FN-row256, NVFP4-G16 and the closed asymmetric K8V4 with
+ * K = FP8-E4M3FN-row256 and V = NVFP4-G16).  Codec rules (the page leaves them
+ * open; this library states them):
+ *   BF16      codes = bf16 bits unchanged.
+ *   INT8-G64  per 64 elements: s = fp16(fp32(amax/127)),
+ *             q = clamp(RNE(x/s), -127, 127); s == 0 -> q = 0.
+ *   FP8-row   per (token, head) row: s = fp16(fp32(amax/448)),
+ *             c = E4M3FN RNE satfinite (x/s); s == 0 -> c = 0.
+ *   NVFP4-G16 per 16 elements: s8 = E4M3FN RNE satfinite (fp32(amax/6)),
+ *             c = E2M1 RNE satfinite (x/s8); s8 == 0 -> c = 0; element 2i in
+ *             the low nibble of byte i.
+ * Quotients are exact quotients rounded once; the sign bit of an E4M3/E2M1
+ * code is the sign of its quotient. */
+typedef enum {
+  NK_BF16 = 0,
+  NK_INT8_G64 = 1,
+  NK_FP8_E4M3_ROW = 2,
+  NK_NVFP4_G16 = 3,
+  NK_K8V4 = 4
+} nk_profile;
+
+/* Plane order ("Paged KV cache" page, closed orders: page-major
+ * [X, P, H, N_physical] for Main/MTP pools, head-major [X, P, N_physical, H]
+ * for the draft pool).  Only page-major is built. */
+typedef enum { NK_PAGE_MAJOR = 0, NK_HEAD_MAJOR = 1 } nk_order;
+
+/* Pool flags.  NK_POOL_CHECK_BOUNDS is accepted for callers that ask for
+ * checked kernels; the range checks described above are always on. */
+enum { NK_POOL_CHECK_BOUNDS = 1 };
+
+/* Geometry of one typed growing pool (capacity section: S = max_context,
+ * C = max_concurrency in 1..8, P = 64, L = ceil(S/P)). */
+typedef struct {
+  int32_t profile;         /* nk_profile                                     */
+  int32_t num_layers;      /* >= 1                                           */
+  int32_t num_kv_heads;    /* H >= 1                                         */
+  int32_t head_dim;        /* D in {64, 128, 256}                            */
+  int32_t max_context;     /* S >= 1                                         */
+  int32_t max_concurrency; /* C in 1..8; block table has C rows of L entries */
+  int32_t order;           /* nk_order; must be NK_PAGE_MAJOR                */
+  int32_t flags;           /* NK_POOL_* bits                                 */
+} nk_pool_desc;
+
+typedef struct nk_pool nk_pool; /* opaque; borrows the caller's planes */
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int nk_version(void);
+
+/* Text of the last error on this thread ("" when none).  Never NULL. */
+const char* nk_last_error(void);
+
+/* Plane inventory of one layer (physical layout section: code plane X = D,
+ * INT8-G64 scale X = D/64, FP8-row scale X = 1, NVFP4 packed codes X = D/2
+ * and scales X = D/16; PageBytes = sum of plane bytes per token * P).
+ * Planes of a profile are ordered [K code, V code, K scale, V scale]; BF16
+ * has only the first two.  Writes *n_planes (2 or 4) and, for each plane, its
+ * byte size for M page groups (bytes[i] = X * elem_bytes * P * H * M) and its
+ * bytes per token per head (row_bytes[i]; may be NULL).  Host only; no CUDA
+ * call.  Errors: NK_ERR_INVALID_ARG, NK_ERR_UNSUPPORTED, NK_ERR_SHAPE. */
+int nk_pool_plane_bytes(const nk_pool_desc* desc, int32_t M, int32_t* n_planes,
+                        size_t bytes[4], size_t row_bytes[4]);
+
+/* Capacity bounds (capacity section): *m_min = max(L, C), *m_max = C * L.
+ * Host only. */
+int nk_pool_capacity_bounds(const nk_pool_desc* desc, int32_t* m_min, int32_t* m_max);
+
+/* Creates a pool handle over caller-owned planes.
+ *   planes: host array of num_layers * n_planes device pointers, layer-major
+ *           (planes[layer * n_planes + i]); each 16-byte aligned and at least
+ *           nk_pool_plane_bytes(...).bytes[i] long.  Their contents are not
+ *           touched; their addresses must stay valid and fixed for the
+ *           handle's lifetime (graph-stable arguments section).
+ *   M:      page groups, within [M_min, M_max] (capacity section).
+ * Must be called with the device that owns the planes current; encodes the
+ * TMA descriptors of every code plane.  The handle is freed by
+ * nk_pool_destroy and owns no device memory.  Errors: NK_ERR_INVALID_ARG,
+ * NK_ERR_UNSUPPORTED, NK_ERR_SHAPE, NK_ERR_RANGE, NK_ERR_ALIGN, NK_ERR_CUDA. */
+int nk_pool_create(const nk_pool_desc* desc, int32_t M, void* const* planes, nk_pool** out);
+
+int nk_pool_destroy(nk_pool* pool);
+
+/* Growing-cache append with fused quantization (persistent codec named by the
+ * page: "kv_cache_append"; translation paragraph of the consumer view
+ * section).  For compact row b (0 <= b < B) and token t < count_b, where
+ * count_b = counts ? counts[b] : T, the token goes to logical position
+ * pos = write_pos[b] + t of table row table_rows[b]:
+ *   g = block_tables[table_rows[b] * L + (pos >> 6)],  o = pos & 63,
+ * and its K and V codes and scales of every KV head h are written at
+ * base + d*nb0 + o*nb1 + h*nb2 + g*nb3 of the layer's planes.
+ *   block_tables: device int32 [C][L];  table_rows, write_pos, counts: device
+ *   int32 [B];  k, v: device bf16 [B][T][H][D] (16-byte aligned).
+ * Writes only the addressed token rows.  Two appends that address the same
+ * (g, o) in one call race.  Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE
+ * (B < 1 or B > C, T < 1, layer out of range), NK_ERR_ALIGN, NK_ERR_CUDA. */
+int nk_paged_kv_append(nk_pool* pool, int32_t layer, const int32_t* block_tables,
+                       const int32_t* table_rows, const int32_t* write_pos,
+                       const int32_t* counts, const void* k, const void* v, int32_t B,
+                       int32_t T, void* stream);
+
+/* Workspace the decode call needs for (B, T, Hq) on the current device. */
+int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t Hq,
+                              size_t* bytes);
+
+/* Compact-batch GQA decode / multi-query verify attention that reads the
+ * pages in place through the block tables (consumer view section, batched
+ * view with table_rows[B]; "no gather-to-contiguous copy").
+ * Row b has valid length F_b = frontiers[b] (which already counts its T new
+ * tokens); query token t of row b attends keys j <= F_b - T + t.  Query head
+ * i uses KV head i / (Hq / H).  Scores s_j = softmax_scale * <q, K^_j>, with
+ * K^ the dequantized keys;  out = softmax(s) V^ ;  lse = ln sum_j exp(s_j).
+ *   q:    device bf16 [B][T][Hq][D];   out: device bf16 [B][T][Hq][D];
+ *   lse:  device fp32 [B][T][Hq] or NULL;  a row with F_b - T + t < 0 gets
+ *         out = 0, lse = -inf.
+ *   workspace: device scratch of at least nk_decode_workspace_bytes bytes
+ *         (split-K partials; contents need no initialisation).
+ * Split-K over pages with a log-sum-exp merge; no host synchronisation, so
+ * the call can be captured in a CUDA graph (graph-stable arguments section).
+ * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T*Hq/H > 64),
+ * NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
+int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,
+                              const int32_t* block_tables, const int32_t* table_rows,
+                              const int32_t* frontiers, int32_t B, int32_t T,
+                              float softmax_scale, void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Workspace the prefill call needs (may be 0). */
+int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32_t Hq,
+                               size_t* bytes);
+
+/* Chunked prefill / replay attention through the block tables (BF16 pools).
+ * Query i < chunk_len[b] of row b sits at logical position prefix_len[b] + i
+ * and attends keys j <= prefix_len[b] + i; the chunk's own K/V must already
+ * be appended.  Prefill work is proportional to prefix*S + S(S+1)/2 query-key
+ * pairs ("Resource scheduling and context cache" page, machine cost model).
+ *   q_chunk: device bf16 [B][Tc][Hq][D];  out: device bf16 [B][Tc][Hq][D]
+ *   (rows i >= chunk_len[b] are not written);  lse: device fp32 [B][Tc][Hq]
+ *   or NULL;  prefix_len, chunk_len: device int32 [B], chunk_len[b] <= Tc.
+ * Errors as for decode; NK_ERR_UNSUPPORTED for non-BF16 pools or D != 256,128. */
+int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const nk_pool* pool,
+                               int32_t layer, const int32_t* block_tables,
+                               const int32_t* table_rows, const int32_t* prefix_len,
+                               const int32_t* chunk_len, int32_t B, int32_t Tc,
+                               float softmax_scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Partial-tail copy-on-write of a Fork (Move/Fork section, worked example
+ * F = 1000: 15 shared full pages, 40 tail columns copied to one private
+ * page).  Copies token columns [0, ncols) of page group src into page group
+ * dst in every plane of every layer; full pages are shared, never copied.
+ * 0 <= ncols <= 64; src != dst; both in [0, M). */
+int nk_page_copy_columns(const nk_pool* pool, int32_t src, int32_t dst, int32_t ncols,
+                         void* stream);
+
+/* Reads (and optionally clears) the device status word of the current device
+ * (NK_STATUS_* bits set by kernels of pools created with
+ * NK_POOL_CHECK_BOUNDS, and by bounded waits that ran out).  Synchronizes
+ * `stream`. */
+int nk_status_read(int32_t* status, int32_t clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NK_H_ */

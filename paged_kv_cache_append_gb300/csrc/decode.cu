@@ -1,0 +1,151 @@
+// decode.cu -- host side of the paged decode attention and the log-sum-exp
+// merge of split-K partials.
+//
+// Merge (split-K over pages): with per-split running max m_s (base 2), sum
+// l_s and unnormalised accumulator acc_s,
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),
+//   out = sum_s acc_s 2^(m_s - M) / L,  lse = (M + log2 L) ln 2,
+// which is exactly the softmax over the union of the splits' keys.
+#include <cmath>
+
+#include "decode.cuh"
+
+namespace nk {
+
+__global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a, int R, int D) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qr = blockIdx.x * 4 + warp;
+  if (qr >= a.T * a.G) return;
+  const int chunk = plan_chunk(a);
+  const int np = (row_frontier(a, b, false) + 63) >> 6;
+  const int ns = (np + chunk - 1) / chunk;
+  if (ns == 1) return;  // the decode CTA of this row wrote out / lse itself
+  const int t = qr / a.G, g = qr % a.G;
+  const int64_t orow = ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g);
+  __nv_bfloat16* out = a.out + orow * D;
+  const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
+  float M = -INFINITY;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(part0 + s) * R + qr].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+  if (M != -INFINITY)
+    for (int s = lane; s < ns; s += 32) {
+      const float2 ml = a.ws_ml[(part0 + s) * R + qr];
+      L += ml.y * ex2(ml.x - M);
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  for (int d = lane; d < D; d += 32) {
+    float acc = 0.f;
+    if (L > 0.f)
+      for (int s = 0; s < ns; ++s) {
+        const float2 ml = a.ws_ml[(part0 + s) * R + qr];
+        acc += a.ws_acc[((part0 + s) * R + qr) * D + d] * ex2(ml.x - M);
+      }
+    out[d] = __float2bfloat16_rn(acc * inv);
+  }
+  if (lane == 0 && a.lse) a.lse[orow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+struct DecodePlan {
+  int nqt, R, target;
+  size_t ws_ml_bytes, ws_bytes;
+  DecodeFn fn;
+};
+
+static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
+  const int H = p->desc.num_kv_heads, D = p->desc.head_dim;
+  if (Hq < 1 || Hq % H) return fail(NK_ERR_SHAPE, "Hq must be a positive multiple of num_kv_heads");
+  if (B < 1 || B > p->desc.max_concurrency) return fail(NK_ERR_SHAPE, "B must be in [1, C]");
+  if (T < 1) return fail(NK_ERR_SHAPE, "T must be >= 1");
+  const int Rr = T * (Hq / H);
+  pl->nqt = Rr <= 8 ? 1 : Rr <= 16 ? 2 : Rr <= 32 ? 4 : 0;
+  if (!pl->nqt) return fail(NK_ERR_UNSUPPORTED, "T * Hq / num_kv_heads must be <= 32");
+  if (D == 256 && pl->nqt == 4)
+    return fail(NK_ERR_UNSUPPORTED, "head_dim 256 supports T * Hq / num_kv_heads <= 16");
+  pl->R = 8 * pl->nqt;
+  OccFn occ;
+  switch (p->desc.profile) {
+    case NK_BF16: pl->fn = decode_bf16; occ = occupancy_bf16; break;
+    case NK_INT8_G64: pl->fn = decode_int8; occ = occupancy_int8; break;
+    case NK_FP8_E4M3_ROW: pl->fn = decode_fp8; occ = occupancy_fp8; break;
+    case NK_NVFP4_G16: pl->fn = decode_nvfp4; occ = occupancy_nvfp4; break;
+    default: pl->fn = decode_k8v4; occ = occupancy_k8v4; break;
+  }
+  const int per_sm = occ(D, pl->nqt);
+  pl->target = p->num_sms * per_sm / H;
+  if (pl->target < 1) pl->target = 1;
+  const size_t parts = static_cast<size_t>(B) * H * pl->target * pl->R;
+  pl->ws_ml_bytes = (parts * sizeof(float2) + 255) / 256 * 256;
+  pl->ws_bytes = pl->ws_ml_bytes + parts * D * sizeof(float);
+  return NK_OK;
+}
+
+}  // namespace nk
+
+using namespace nk;
+
+extern "C" int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t Hq,
+                                         size_t* bytes) {
+  clear_error();
+  if (!pool || !bytes) return fail(NK_ERR_INVALID_ARG, "null argument");
+  DecodePlan pl;
+  int rc = make_plan(pool, B, T, Hq, &pl);
+  if (rc) return rc;
+  *bytes = pl.ws_bytes;
+  return NK_OK;
+}
+
+extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool,
+                                         int32_t layer, const int32_t* block_tables,
+                                         const int32_t* table_rows, const int32_t* frontiers,
+                                         int32_t B, int32_t T, float softmax_scale, void* out,
+                                         float* lse, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  clear_error();
+  if (!q || !pool || !block_tables || !table_rows || !frontiers || !out)
+    return fail(NK_ERR_INVALID_ARG, "null argument to nk_paged_decode_attention");
+  if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
+  if (!aligned16(q) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
+  DecodePlan pl;
+  int rc = make_plan(pool, B, T, Hq, &pl);
+  if (rc) return rc;
+  if (!workspace || workspace_bytes < pl.ws_bytes)
+    return fail(NK_ERR_WORKSPACE, "workspace needs " + std::to_string(pl.ws_bytes) + " bytes");
+  if (!aligned16(workspace)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
+  DecodeArgs a;
+  const int np = pool->n_planes;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.tables = block_tables;
+  a.table_rows = table_rows;
+  a.frontiers = frontiers;
+  a.ks = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 2]) : nullptr;
+  a.vs = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.ws_ml = static_cast<float2*>(workspace);
+  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.ws_ml_bytes);
+  a.status = pool->status;
+  a.softmax_scale = softmax_scale;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.H = pool->desc.num_kv_heads;
+  a.G = Hq / a.H;
+  a.L = pool->L;
+  a.M = pool->M;
+  a.C = pool->desc.max_concurrency;
+  a.target = pl.target;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  const int Rr = T * a.G;
+  merge_kernel<<<dim3((Rr + 3) / 4, a.H, B), 128, 0, s>>>(a, pl.R, pool->desc.head_dim);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return NK_OK;
+}
