@@ -187,6 +187,29 @@ int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, in
                               float softmax_scale, void* out, float* lse, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Size of the static device scratch of nk_paged_decode_attention_noalloc. */
+#define NK_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* nk_paged_decode_attention for callers that cannot allocate device memory
+ * (allocator callbacks, runtimes with a memory budget fixed at start-up,
+ * loops that must never block on the driver's allocator).  The design page
+ * has no counterpart: this is an interface choice of this library.
+ * Same arguments, results and errors as nk_paged_decode_attention, without
+ * the workspace: the split-K partials live in a static device array of
+ * NK_NOALLOC_SCRATCH_BYTES (32 MiB) that every device that loads this entry
+ * point keeps until the process exits.  The number of splits is lowered
+ * until the partials fit; a call that does not fit even with one split per
+ * (row, KV head) is rejected with NK_ERR_WORKSPACE before any launch.
+ * The first call on a device (with that device current, which must be the
+ * pool's device) looks up the array's device address; make it before any
+ * stream capture.  All calls share the array: two calls that overlap on the
+ * GPU race.  Calls no allocating routine. */
+int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* pool,
+                                      int32_t layer, const int32_t* block_tables,
+                                      const int32_t* table_rows, const int32_t* frontiers,
+                                      int32_t B, int32_t T, float softmax_scale, void* out,
+                                      float* lse, void* stream);
+
 /* Workspace the prefill call needs (may be 0). */
 int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32_t Hq,
                                size_t* bytes);

@@ -149,3 +149,66 @@ extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_poo
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return NK_OK;
 }
+
+namespace nk {
+
+// Decode + merge whose split-K partials live in a caller-given scratch area
+// of at most `max_ws` bytes: the split target is lowered until the partials
+// fit.  Used by the entry point that allocates nothing (decode_noalloc.cu).
+int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,
+                        const int32_t* block_tables, const int32_t* table_rows,
+                        const int32_t* frontiers, int32_t B, int32_t T, float softmax_scale,
+                        void* out, float* lse, void* scratch, size_t max_ws, cudaStream_t s) {
+  if (!q || !pool || !block_tables || !table_rows || !frontiers || !out || !scratch)
+    return fail(NK_ERR_INVALID_ARG, "null argument to the static-scratch decode");
+  if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
+  if (!aligned16(q) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
+  DecodePlan pl;
+  int rc = make_plan(pool, B, T, Hq, &pl);
+  if (rc) return rc;
+  const int H = pool->desc.num_kv_heads, D = pool->desc.head_dim;
+  const size_t per_split = static_cast<size_t>(B) * H * pl.R * (sizeof(float2) + D * sizeof(float));
+  if (pl.ws_bytes > max_ws) {
+    const size_t fit = (max_ws - 256) / per_split;
+    if (fit < 1)
+      return fail(NK_ERR_WORKSPACE, "one split of this call needs " + std::to_string(per_split + 256) +
+                                        " bytes of scratch; the static scratch holds " +
+                                        std::to_string(max_ws));
+    pl.target = static_cast<int>(fit < static_cast<size_t>(pl.target) ? fit : pl.target);
+    const size_t parts = static_cast<size_t>(B) * H * pl.target * pl.R;
+    pl.ws_ml_bytes = (parts * sizeof(float2) + 255) / 256 * 256;
+    pl.ws_bytes = pl.ws_ml_bytes + parts * D * sizeof(float);
+  }
+  DecodeArgs a;
+  const int np = pool->n_planes;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.tables = block_tables;
+  a.table_rows = table_rows;
+  a.frontiers = frontiers;
+  a.ks = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 2]) : nullptr;
+  a.vs = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.ws_ml = static_cast<float2*>(scratch);
+  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(scratch) + pl.ws_ml_bytes);
+  a.status = pool->status;
+  a.softmax_scale = softmax_scale;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.H = H;
+  a.G = Hq / H;
+  a.L = pool->L;
+  a.M = pool->M;
+  a.C = pool->desc.max_concurrency;
+  a.target = pl.target;
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  merge_kernel<<<dim3((T * a.G + 3) / 4, a.H, B), 128, 0, s>>>(a, pl.R, D);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return NK_OK;
+}
+
+}  // namespace nk

@@ -27,7 +27,8 @@ POOL_CHECK_BOUNDS = 1
 
 SYMBOLS = ["nk_version", "nk_last_error", "nk_pool_plane_bytes", "nk_pool_capacity_bounds",
            "nk_pool_create", "nk_pool_destroy", "nk_paged_kv_append", "nk_decode_workspace_bytes",
-           "nk_paged_decode_attention", "nk_prefill_workspace_bytes", "nk_paged_prefill_attention",
+           "nk_paged_decode_attention", "nk_paged_decode_attention_noalloc",
+           "nk_prefill_workspace_bytes", "nk_paged_prefill_attention",
            "nk_page_copy_columns", "nk_status_read"]
 
 
@@ -66,6 +67,7 @@ def load(path: str | None = None) -> C.CDLL:
         "nk_paged_kv_append": (C.c_int, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
         "nk_decode_workspace_bytes": (C.c_int, [_P, _I, _I, _I, C.POINTER(_S)]),
         "nk_paged_decode_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
+        "nk_paged_decode_attention_noalloc": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P]),
         "nk_prefill_workspace_bytes": (C.c_int, [_P, _I, _I, _I, C.POINTER(_S)]),
         "nk_paged_prefill_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
         "nk_page_copy_columns": (C.c_int, [_P, _I, _I, _I, _P]),
@@ -135,6 +137,12 @@ def nk_paged_decode_attention(q, Hq, pool, layer, block_tables, table_rows, fron
                               out, lse, workspace, workspace_bytes, stream):
     _check(load().nk_paged_decode_attention(q, Hq, pool, layer, block_tables, table_rows, frontiers,
                                             B, T, scale, out, lse, workspace, workspace_bytes, stream))
+
+
+def nk_paged_decode_attention_noalloc(q, Hq, pool, layer, block_tables, table_rows, frontiers, B, T,
+                                      scale, out, lse, stream):
+    _check(load().nk_paged_decode_attention_noalloc(q, Hq, pool, layer, block_tables, table_rows,
+                                                    frontiers, B, T, scale, out, lse, stream))
 
 
 def nk_prefill_workspace_bytes(pool, B, Tc, Hq) -> int:
