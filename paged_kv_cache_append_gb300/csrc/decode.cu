@@ -12,42 +12,84 @@
 
 namespace nk {
 
+// One CTA per (64 head dims, KV head, row).  Warps first turn each query's
+// split statistics into weights w_s = 2^(m_s - M) / L (shared memory), then
+// every thread sums weighted partials for a few (query, dim) outputs with
+// coalesced loads over the dims.
+constexpr int kMergeDims = 64;
+
 __global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a, int R, int D) {
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qr = blockIdx.x * 4 + warp;
-  if (qr >= a.T * a.G) return;
-  const int chunk = plan_chunk(a);
-  const int np = (row_frontier(a, b, false) + 63) >> 6;
-  const int ns = (np + chunk - 1) / chunk;
-  if (ns == 1) return;  // the decode CTA of this row wrote out / lse itself
-  const int t = qr / a.G, g = qr % a.G;
-  const int64_t orow = ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g);
-  __nv_bfloat16* out = a.out + orow * D;
-  const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(part0 + s) * R + qr].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f;
-  if (M != -INFINITY)
-    for (int s = lane; s < ns; s += 32) {
-      const float2 ml = a.ws_ml[(part0 + s) * R + qr];
-      L += ml.y * ex2(ml.x - M);
-    }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  for (int d = lane; d < D; d += 32) {
-    float acc = 0.f;
-    if (L > 0.f)
-      for (int s = 0; s < ns; ++s) {
-        const float2 ml = a.ws_ml[(part0 + s) * R + qr];
-        acc += a.ws_acc[((part0 + s) * R + qr) * D + d] * ex2(ml.x - M);
-      }
-    out[d] = __float2bfloat16_rn(acc * inv);
+  extern __shared__ float w_s[];  // [T*G][target]
+  __shared__ int s_F[8];
+  const int b = blockIdx.z, h = blockIdx.y, d0 = blockIdx.x * kMergeDims;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < a.B) {
+    const int F = a.frontiers[tid], row = a.table_rows[tid];
+    s_F[tid] = (F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C) ? F : 0;
   }
-  if (lane == 0 && a.lse) a.lse[orow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  __syncthreads();
+  int total = 0;
+  for (int bb = 0; bb < a.B; ++bb) total += (s_F[bb] + 63) >> 6;
+  const int chunk = max(1, (total + a.target - 1) / a.target);
+  const int ns = (((s_F[b] + 63) >> 6) + chunk - 1) / chunk;
+  if (ns == 1) return;  // the decode CTA of this row wrote out / lse itself
+  const int Rr = a.T * a.G;
+  const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
+  for (int qr = warp; qr < Rr; qr += 4) {
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(part0 + s) * R + qr].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int s = lane; s < ns; s += 32) {
+        const float2 ml = a.ws_ml[(part0 + s) * R + qr];
+        L += ml.y * ex2(ml.x - M);
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int s = lane; s < ns; s += 32)
+      w_s[qr * a.target + s] = L > 0.f ? ex2(a.ws_ml[(part0 + s) * R + qr].x - M) * inv : 0.f;
+    if (lane == 0 && blockIdx.x == 0 && a.lse) {
+      const int t = qr / a.G, g = qr % a.G;
+      a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
+          L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  const int nd = min(kMergeDims, D - d0);
+  for (int i = tid; i < Rr * nd; i += 128) {
+    const int qr = i / nd, d = d0 + i % nd;
+    const float* src = a.ws_acc + (part0 * R + qr) * D + d;
+    const float* w = w_s + qr * a.target;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= ns; s += 4) {
+      acc0 = fmaf(w[s], src[static_cast<int64_t>(s) * R * D], acc0);
+      acc1 = fmaf(w[s + 1], src[static_cast<int64_t>(s + 1) * R * D], acc1);
+      acc2 = fmaf(w[s + 2], src[static_cast<int64_t>(s + 2) * R * D], acc2);
+      acc3 = fmaf(w[s + 3], src[static_cast<int64_t>(s + 3) * R * D], acc3);
+    }
+    for (; s < ns; ++s) acc0 = fmaf(w[s], src[static_cast<int64_t>(s) * R * D], acc0);
+    const int t = qr / a.G, g = qr % a.G;
+    a.out[((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d] =
+        __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
+  }
+}
+
+// Launches the merge; its dynamic shared memory holds T*G x target weights.
+static cudaError_t launch_merge(const DecodeArgs& a, int R, int D, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(a.T) * a.G * a.target * sizeof(float);
+  static size_t attr = 0;
+  if (smem > 48 * 1024 && smem > attr) {
+    cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = smem;
+  }
+  merge_kernel<<<dim3((D + kMergeDims - 1) / kMergeDims, a.H, a.B), 128, smem, s>>>(a, R, D);
+  return cudaGetLastError();
 }
 
 struct DecodePlan {
@@ -143,9 +185,7 @@ extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_poo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  const int Rr = T * a.G;
-  merge_kernel<<<dim3((Rr + 3) / 4, a.H, B), 128, 0, s>>>(a, pl.R, pool->desc.head_dim);
-  e = cudaGetLastError();
+  e = launch_merge(a, pl.R, pool->desc.head_dim, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return NK_OK;
 }
@@ -205,8 +245,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.target = pl.target;
   cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  merge_kernel<<<dim3((T * a.G + 3) / 4, a.H, B), 128, 0, s>>>(a, pl.R, D);
-  e = cudaGetLastError();
+  e = launch_merge(a, pl.R, D, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return NK_OK;
 }

@@ -7,25 +7,31 @@
 // inner loop), with no gather-to-contiguous copy; a frontier may sit at any
 // offset of the last page and bytes past it are never used.
 //
-// Work split.  A CTA (4 warps) owns one (row b, KV head h, page range).  The
-// page ranges come from the device-side frontiers, so the host needs no
-// lengths and the launch is graph-stable: with N_b = ceil(F_b / 64) pages,
-// every CTA computes chunk = ceil(sum_b N_b / target), row b gets
-// ceil(N_b / chunk) splits, and CTA x of a head takes the x-th split.
+// Work split.  A CTA owns one (row b, KV head h, page range).  The page
+// ranges come from the device-side frontiers, so the host needs no lengths and
+// the launch is graph-stable: with N_b = ceil(F_b / 64) pages, every CTA
+// computes chunk = ceil(sum_b N_b / target), row b gets ceil(N_b / chunk)
+// splits, and CTA x of a head takes the x-th split.
 //
-// Per page (64 keys), staged by TMA into a ring of NSTAGE shared buffers:
-//  QK:  warp w takes keys [16w, 16w+16): S^T(16 keys x R queries) via
-//       mma.m16n8k16 with the K tile as the A operand (ldmatrix of the raw
-//       codes, exact conversion to f16/bf16 in registers) and q as B.
-//       INT8-G64 group scales and FP8 row scales multiply the fp32 partial
-//       sums; NVFP4 scales multiply the f16 operand (exact product).
-//  softmax: base-2 online softmax, CTA-wide running max per query through
-//       shared memory; P (f16 / bf16) goes to shared memory.
-//  PV:  warp w takes head dims [w*D/4, (w+1)*D/4): O^T += V^T P^T, V^T built
-//       in registers from the V tile (ldmatrix.trans for bf16; byte gathers
-//       for 8-bit and 4-bit codes), V scales folded in as f16 products.
-// The CTA writes unnormalised partials (m, l, acc) to the workspace, or the
-// final out / lse when its row has a single split.
+// Warp roles (160 threads).  Warp 4 is the producer: one lane stages page
+// tiles (K codes, V codes, K / V scales of one (page, head)) into a ring of
+// NSTAGE shared buffers with TMA / bulk copies, tracked by full / empty
+// mbarriers.  Warps 0..3 are consumers; consumer w owns keys [16w, 16w+16) of
+// every page and keeps its own online softmax, so the loop has no CTA-wide
+// barrier:
+//  QK:  S^T (16 keys x R query rows) by mma.m16n8k16 with the K tile as the A
+//       operand (ldmatrix of the raw codes, exact conversion to f16 / bf16 in
+//       registers) and q as B.  INT8-G64 group scales and FP8 row scales
+//       multiply the fp32 partial sums; NVFP4 scales multiply the f16 operand
+//       (exact product).
+//  softmax: base-2, running max per query row over the warp's keys.
+//  PV:  O^T (all D dims x R) += V^T P^T with P^T taken straight from the S
+//       registers by movmatrix, V^T built in registers from the V tile
+//       (ldmatrix.trans for bf16; byte gathers for 8-bit and 4-bit codes), V
+//       scales folded in as f16 products.
+// At the end the four warps' (m, l, O) are combined in a fixed order, and the
+// CTA writes unnormalised partials (m, l, acc) to the workspace, or the final
+// out / lse when its row has a single split.
 #pragma once
 
 #include "device.cuh"
@@ -53,26 +59,6 @@ struct DecodeArgs {
   int target;    // splits per head the chunking aims at (= maxsplit)
 };
 
-// Valid length of compact row b.  A table row outside [0, C) or a frontier
-// outside [0, L*64] never leads to an out-of-bounds access: the row is read as
-// empty and NK_STATUS_FRONTIER is recorded (by one thread, when `flag`).
-__device__ __forceinline__ int row_frontier(const DecodeArgs& a, int b, bool flag) {
-  const int F = a.frontiers[b];
-  const int row = a.table_rows[b];
-  if (F < 0 || F > a.L * 64 || row < 0 || row >= a.C) {
-    if (flag) set_status(a.status, NK_STATUS_FRONTIER);
-    return 0;
-  }
-  return F;
-}
-
-__device__ __forceinline__ int plan_chunk(const DecodeArgs& a, bool flag = false) {
-  int total = 0;
-  for (int b = 0; b < a.B; ++b) total += (row_frontier(a, b, flag) + 63) >> 6;
-  const int chunk = (total + a.target - 1) / a.target;
-  return chunk < 1 ? 1 : chunk;
-}
-
 template <int KIND>
 struct CodeRow {
   static constexpr int bytes(int D) { return KIND == KIND_BF16 ? 2 * D : KIND == KIND_NVFP4 ? D / 2 : D; }
@@ -88,7 +74,8 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int KK, int KV, int D, int NQT>
 struct DecodeCfg {
-  static constexpr int R = 8 * NQT;  // query rows (T * G) padded to n-tiles of 8
+  static constexpr int THREADS = 160;  // 4 consumer warps + 1 producer warp
+  static constexpr int R = 8 * NQT;    // query rows (T * G) padded to n-tiles of 8
   static constexpr int KCB = CodeRow<KK>::bytes(D);
   static constexpr int VCB = CodeRow<KV>::bytes(D);
   static constexpr int KSB = ScaleRow<KK>::bytes(D);
@@ -102,24 +89,21 @@ struct DecodeCfg {
   static constexpr int OFF_VS = OFF_KS + align_up(KS_TILE, 128);
   static constexpr int STAGE = align_up(OFF_VS + VS_TILE, 1024);
   static constexpr int TX_BYTES = K_TILE + V_TILE + KS_TILE + VS_TILE;
-  // Ring depth: three 64 KB stages (one CTA per SM) for BF16 D=256, else as
-  // many stages as fit in ~104 KB so that two CTAs share an SM.
-  static constexpr int NSTAGE =
-      STAGE > 48 * 1024 ? 3 : (104 * 1024 / STAGE < 2 ? 2 : (104 * 1024 / STAGE > 8 ? 8 : 104 * 1024 / STAGE));
-  static constexpr int P_PITCH = 64 * 2 + 16;  // bytes per query row of P (padded)
-  // BF16 pools run PV in bf16: P is kept as hi + lo bf16 parts (about 16
-  // significant bits), the f16 paths keep one f16 P.
-  static constexpr int NPBUF = (KK == KIND_BF16) ? 2 : 1;
-  static constexpr int P_BUF = align_up(R * P_PITCH, 128);
-  static constexpr int OFF_P = NSTAGE * STAGE;
-  static constexpr int OFF_RED = OFF_P + NPBUF * P_BUF;
-  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * R * 4;
-  static constexpr int SMEM = OFF_BAR + NSTAGE * 8 + 32 + 1024;  // + alignment slack
+  // Ring depth: four stages of small tiles (several CTAs per SM), two of the
+  // larger ones.
+  static constexpr int NSTAGE = STAGE <= 16 * 1024 ? 4 : 2;
   static constexpr bool MMA_BF16 = (KK == KIND_BF16);
   static constexpr int KSTEPS = D / 16;
-  static constexpr int DW = D / 4;     // head dims per warp in PV
-  static constexpr int MT = DW / 16;   // m-tiles per warp in PV
-  static constexpr int EPT = DW >= 32 ? 4 : 2;  // V elements gathered per key per thread
+  static constexpr int MT = D / 16;  // m-tiles of PV (all head dims per warp)
+  // q fragments live in registers when they are few, else in shared memory
+  static constexpr bool Q_SMEM = KSTEPS * NQT * 2 > 32;
+  static constexpr int Q_PITCH = D * 2 + 32;  // bytes per q row (padded against bank conflicts)
+  static constexpr int OFF_Q = NSTAGE * STAGE;
+  static constexpr int OFF_RED = OFF_Q + align_up(R * Q_PITCH, 128);
+  static constexpr int OFF_BAR = OFF_RED + 4 * 4 * R * 4;  // m, l per warp; M, L per row
+  static constexpr int MISC_INTS = 32;
+  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
+  static_assert(R * D * 4 <= NSTAGE * STAGE, "final combine reuses the stage ring");
 };
 
 // d index of the q element in slot i (0..3: b0.lo, b0.hi, b1.lo, b1.hi) of
@@ -139,8 +123,21 @@ __device__ __forceinline__ uint32_t cvt_pair(uint32_t w) {
   else return e4m3x2_to_f16x2(static_cast<uint16_t>(HI ? (w >> 16) : (w & 0xFFFFu)));
 }
 
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Barrier of the four consumer warps only (named barrier 1).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <int KK, int KV, int D, int NQT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(160)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeArgs a) {
   using Cfg = DecodeCfg<KK, KV, D, NQT>;
@@ -148,23 +145,51 @@ __global__ void __launch_bounds__(128)
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Ps = smem + Cfg::OFF_P;
-  float* red_max = reinterpret_cast<float*>(smem + Cfg::OFF_RED);  // [4][R]
-  float* red_l = red_max + 4 * R;                                  // [4][R]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  int* s_flags = reinterpret_cast<int*>(bars + NSTAGE);             // [0] abort
+  uint8_t* qs = smem + Cfg::OFF_Q;                                  // q rows [R][Q_PITCH]
+  float* red_m = reinterpret_cast<float*>(smem + Cfg::OFF_RED);    // [4][R]
+  float* red_l = red_m + 4 * R;                                     // [4][R]
+  float* row_M = red_l + 4 * R;                                     // [R]
+  float* row_L = row_M + R;                                         // [R]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  uint64_t* empty = full + NSTAGE;
+  int* s_flags = reinterpret_cast<int*>(empty + NSTAGE);  // [0] abort
+  int* s_F = s_flags + 4;                                 // [8] valid length per row
+  int* s_row = s_flags + 12;                              // [8] table row per row
+  float* s_qmax = reinterpret_cast<float*>(s_flags + 20); // [4] per-warp max|q|
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int h = blockIdx.y;
 
-  // ---- which (row, split) this CTA owns --------------------------------
-  const int chunk = plan_chunk(a, tid == 0 && blockIdx.x == 0 && h == 0);
+  // ---- per-row lengths, loaded once in parallel ------------------------------
+  if (tid < a.B) {
+    const int F = a.frontiers[tid], row = a.table_rows[tid];
+    const bool ok = F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C;
+    if (!ok && blockIdx.x == 0 && h == 0) set_status(a.status, NK_STATUS_FRONTIER);
+    s_F[tid] = ok ? F : 0;
+    s_row[tid] = ok ? row : 0;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    s_flags[0] = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  __syncthreads();
+
+  // ---- which (row, split) this CTA owns --------------------------------------
+  int total = 0;
+  for (int bb = 0; bb < a.B; ++bb) total += (s_F[bb] + 63) >> 6;
+  const int chunk = max(1, (total + a.target - 1) / a.target);
   int b = -1, split = 0, nsplit = 0, npages = 0;
   {
     int acc = 0;
     for (int bb = 0; bb < a.B; ++bb) {
-      const int np = (row_frontier(a, bb, false) + 63) >> 6;
+      const int np = (s_F[bb] + 63) >> 6;
       const int ns = (np + chunk - 1) / chunk;
       if (static_cast<int>(blockIdx.x) < acc + ns) {
         b = bb;
@@ -177,103 +202,129 @@ __global__ void __launch_bounds__(128)
     }
   }
   if (b < 0) return;
-  const int F = row_frontier(a, b, false);
+  const int F = s_F[b];
   const int p0 = split * chunk;
   const int n = min(chunk, npages - p0);  // pages of this CTA (>= 1)
-  const int32_t* table = a.tables + static_cast<int64_t>(a.table_rows[b]) * a.L;
   const int R_real = a.T * a.G;
 
-  if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
-    s_flags[0] = 0;
-    fence_barrier_init();
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-  }
-  __syncthreads();
-
-  // Producer: thread 0 stages page p0 + i into stage i % NSTAGE.
-  auto issue = [&](int i) {
-    const int s = i % NSTAGE;
-    int g = table[p0 + i];
-    if (g < 0 || g >= a.M) {  // never copy from outside the pool
-      set_status(a.status, NK_STATUS_PAGE_RANGE);
-      g = 0;                  // the row's result is then undefined
-    }
-    uint8_t* st = smem + s * Cfg::STAGE;
-    const int y = (g * a.H + h) * 64;
-    mbar_arrive_expect_tx(&bars[s], Cfg::TX_BYTES);
-#pragma unroll
-    for (int j = 0; j < Cfg::KCB / Cfg::K_RB; ++j) tma_load_2d(st + j * 64 * Cfg::K_RB, &tmk, j * Cfg::K_RB, y, &bars[s]);
-#pragma unroll
-    for (int j = 0; j < Cfg::VCB / Cfg::V_RB; ++j)
-      tma_load_2d(st + Cfg::OFF_V + j * 64 * Cfg::V_RB, &tmv, j * Cfg::V_RB, y, &bars[s]);
-    if constexpr (Cfg::KS_TILE > 0) {
-      bulk_load(st + Cfg::OFF_KS, a.ks + static_cast<int64_t>(y) * Cfg::KSB, Cfg::KS_TILE, &bars[s]);
-      bulk_load(st + Cfg::OFF_VS, a.vs + static_cast<int64_t>(y) * Cfg::VSB, Cfg::VS_TILE, &bars[s]);
-    }
-  };
-  int issued = 0;
-  if (tid == 0) {
-    for (; issued < NSTAGE && issued < n; ++issued) issue(issued);
-  }
-
-  // ---- q fragments (B operand of QK) ----------------------------------------
-  // Quantized profiles run the MMAs in f16: q is scaled by 2^e so that
-  // max|q| * 2^e lies in [2^14, 2^15) (exact for every element above
-  // max|q| * 2^-31), and the scores divide 2^e back out.
-  uint32_t qf[Cfg::KSTEPS][NQT][2];
-  float qscale_log2 = 0.f;
-  {
-    auto qrow_ptr = [&](int j, bool& live) {
-      const int qr = 8 * j + r;
-      live = qr < R_real;
-      const int t = live ? qr / a.G : 0, g = live ? qr % a.G : 0;
-      return a.q + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D;
-    };
-    float f = 1.f;
-    if constexpr (!Cfg::MMA_BF16) {
-      float mx = 0.f;
-#pragma unroll
-      for (int j = 0; j < NQT; ++j) {
-        bool live;
-        const __nv_bfloat16* qp = qrow_ptr(j, live);
-        if (live)
-#pragma unroll
-          for (int s = 0; s < Cfg::KSTEPS; ++s)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(__bfloat162float(qp[q_dim<KK>(s, i, c)])));
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      int ex = 0;
-      if (mx > 0.f) frexpf(mx, &ex);
-      const int e = mx > 0.f ? 15 - ex : 0;
-      f = ldexpf(1.f, e);
-      qscale_log2 = static_cast<float>(e);
-    }
-#pragma unroll
-    for (int j = 0; j < NQT; ++j) {
-      bool live;
-      const __nv_bfloat16* qp = qrow_ptr(j, live);
-#pragma unroll
-      for (int s = 0; s < Cfg::KSTEPS; ++s) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = live ? __bfloat162float(qp[q_dim<KK>(s, i, c)]) * f : 0.f;
-        if constexpr (Cfg::MMA_BF16) {
-          qf[s][j][0] = pack_bf16x2(v[0], v[1]);
-          qf[s][j][1] = pack_bf16x2(v[2], v[3]);
+  // ---- producer warp: stage pages p0 .. p0+n-1 ---------------------------------
+  if (warp == 4) {
+    const int32_t* table = a.tables + static_cast<int64_t>(s_row[b]) * a.L + p0;
+    int gnext = 0;
+    for (int i = 0; i < n; ++i) {
+      if ((i & 31) == 0) gnext = (i + lane < n) ? table[i + lane] : 0;  // 32 table entries per load
+      int g = __shfl_sync(0xffffffffu, gnext, i & 31);
+      int stop = 0;
+      if (lane == 0) {
+        const int s = i % NSTAGE;
+        if (i >= NSTAGE && !mbar_wait_bounded(&empty[s], ((i / NSTAGE) - 1) & 1, a.status)) {
+          s_flags[0] = 1;
+          stop = 1;
         } else {
-          qf[s][j][0] = pack_f16x2(v[0], v[1]);
-          qf[s][j][1] = pack_f16x2(v[2], v[3]);
+          if (g < 0 || g >= a.M) {  // never copy from outside the pool
+            set_status(a.status, NK_STATUS_PAGE_RANGE);
+            g = 0;                  // the row's result is then undefined
+          }
+          uint8_t* st = smem + s * Cfg::STAGE;
+          const int y = (g * a.H + h) * 64;
+          mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+#pragma unroll
+          for (int j = 0; j < Cfg::KCB / Cfg::K_RB; ++j)
+            tma_load_2d(st + j * 64 * Cfg::K_RB, &tmk, j * Cfg::K_RB, y, &full[s]);
+#pragma unroll
+          for (int j = 0; j < Cfg::VCB / Cfg::V_RB; ++j)
+            tma_load_2d(st + Cfg::OFF_V + j * 64 * Cfg::V_RB, &tmv, j * Cfg::V_RB, y, &full[s]);
+          if constexpr (Cfg::KS_TILE > 0) {
+            bulk_load(st + Cfg::OFF_KS, a.ks + static_cast<int64_t>(y) * Cfg::KSB, Cfg::KS_TILE, &full[s]);
+            bulk_load(st + Cfg::OFF_VS, a.vs + static_cast<int64_t>(y) * Cfg::VSB, Cfg::VS_TILE, &full[s]);
+          }
         }
       }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+    }
+    return;  // the copies complete into the shared memory of the still-running CTA
+  }
+
+  // ---- q rows to shared memory (16-byte loads) and the f16 prescale --------------
+  // Row qr = t * G + g of this CTA is q[b][t][h * G + g][:]; the G rows of one
+  // token are contiguous.  Padded rows (qr >= T * G) are zero.  Quantized
+  // profiles run the MMAs in f16: q is scaled by 2^e so that max|q| * 2^e lies
+  // in [2^14, 2^15) (exact for every element above max|q| * 2^-31), and the
+  // scores divide 2^e back out.
+  float mx = 0.f;
+  {
+    constexpr int V8 = D / 8;  // uint4 per row
+    for (int i = tid; i < R * V8; i += 128) {
+      const int qr = i / V8, col = i % V8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qr < R_real) {
+        const int t = qr / a.G, g = qr % a.G;
+        v = *reinterpret_cast<const uint4*>(
+            a.q + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + col * 8);
+      }
+      *reinterpret_cast<uint4*>(qs + qr * Cfg::Q_PITCH + col * 16) = v;
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(__bfloat162float(e[k])));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) s_qmax[warp] = mx;
+  }
+  consumer_sync();
+  mx = fmaxf(fmaxf(s_qmax[0], s_qmax[1]), fmaxf(s_qmax[2], s_qmax[3]));
+  float qscale_log2 = 0.f, qf_mul = 1.f;
+  if constexpr (!Cfg::MMA_BF16) {
+    int ex = 0;
+    if (mx > 0.f) frexpf(mx, &ex);
+    const int e = mx > 0.f ? 15 - ex : 0;
+    qf_mul = ldexpf(1.f, e);
+    qscale_log2 = static_cast<float>(e);
+    if constexpr (Cfg::Q_SMEM) {  // convert in place to f16
+      for (int i = tid; i < R * D / 2; i += 128) {
+        const int qr = i / (D / 2), col = i % (D / 2);
+        uint32_t* p = reinterpret_cast<uint32_t*>(qs + qr * Cfg::Q_PITCH + col * 4);
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+        *p = pack_f16x2(__low2float(v) * qf_mul, __high2float(v) * qf_mul);
+      }
+      consumer_sync();
     }
   }
   const float sc = a.softmax_scale * kLog2e * exp2f(-qscale_log2);
 
-  // ---- running state -----------------------------------------------------
+  // q fragment of k-step s, n-tile j: (b0, b1) read from shared memory
+  auto qfrag = [&](int s, int j, uint32_t& b0, uint32_t& b1) {
+    const uint8_t* row = qs + (8 * j + r) * Cfg::Q_PITCH;
+    if constexpr (KK == KIND_BF16) {
+      b0 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(s, 0, c));
+      b1 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(s, 2, c));
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(row + 2 * q_dim<KK>(s, 0, c));
+      b0 = v.x;
+      b1 = v.y;
+    }
+  };
+  uint32_t qreg[Cfg::Q_SMEM ? 1 : Cfg::KSTEPS][Cfg::Q_SMEM ? 1 : NQT][2];
+  if constexpr (!Cfg::Q_SMEM) {
+#pragma unroll
+    for (int s = 0; s < Cfg::KSTEPS; ++s)
+#pragma unroll
+      for (int j = 0; j < NQT; ++j) {
+        if constexpr (Cfg::MMA_BF16) {
+          qfrag(s, j, qreg[s][j][0], qreg[s][j][1]);
+        } else {
+          const uint8_t* row = qs + (8 * j + r) * Cfg::Q_PITCH;
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(row + 2 * q_dim<KK>(s, i, c))) * qf_mul;
+          qreg[s][j][0] = pack_f16x2(v[0], v[1]);
+          qreg[s][j][1] = pack_f16x2(v[2], v[3]);
+        }
+      }
+  }
+
+  // ---- running state -----------------------------------------------------------
   float m_run[NQT][2], l_part[NQT][2];
   float o[Cfg::MT][NQT][4];
 #pragma unroll
@@ -286,32 +337,34 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int j = 0; j < NQT; ++j) o[mt][j][0] = o[mt][j][1] = o[mt][j][2] = o[mt][j][3] = 0.f;
 
-  // query-token limits: query row q may see keys <= F - T + q / G (and < F)
+  // query row qr may see keys <= F - T + qr / G (and < F)
   int lim[NQT][2];
 #pragma unroll
   for (int j = 0; j < NQT; ++j)
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int qr = 8 * j + 2 * c + u;
-      lim[j][u] = min(F - a.T + qr / a.G, F - 1);
-    }
+    for (int u = 0; u < 2; ++u) lim[j][u] = min(F - a.T + (8 * j + 2 * c + u) / a.G, F - 1);
+
+  const int kr0 = 16 * warp + r, kr1 = kr0 + 8;                        // keys of this thread's S rows
+  const int krow_ld = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row of this lane
+  const int kk0 = 16 * warp + 2 * c;                                   // first PV key of this thread
 
   bool aborted = false;
-  for (int i = 0; i < n; ++i) {
+  int i = 0;
+  for (; i < n; ++i) {
     const int s = i % NSTAGE;
     const uint8_t* st = smem + s * Cfg::STAGE;
     const uint32_t kbase = smem_u32(st);
     const uint32_t vbase = smem_u32(st + Cfg::OFF_V);
-    if (!mbar_wait_bounded(&bars[s], (i / NSTAGE) & 1, a.status)) s_flags[0] = 1;
-    const int page = p0 + i;
-    const int key0 = page * 64;
+    if (!mbar_wait_bounded(&full[s], (i / NSTAGE) & 1, a.status)) {
+      aborted = true;
+      break;
+    }
+    const int key0 = (p0 + i) * 64;
 
-    // ---------------- QK: S^T for keys [16*warp, 16*warp+16) -------------
+    // ---------------- QK: S^T for this warp's 16 keys ------------------------------
     float S[NQT][4];
 #pragma unroll
     for (int j = 0; j < NQT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
-    const int krow_ld = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row of this lane
-    const int kr0 = 16 * warp + r, kr1 = kr0 + 8;                      // keys of this thread's S rows
     if constexpr (KK == KIND_BF16) {
 #pragma unroll
       for (int s16 = 0; s16 < Cfg::KSTEPS; ++s16) {
@@ -320,7 +373,12 @@ __global__ void __launch_bounds__(128)
         uint32_t A[4];
         ldsm_x4(addr, A[0], A[1], A[2], A[3]);
 #pragma unroll
-        for (int j = 0; j < NQT; ++j) mma16816<true>(S[j], A, qf[s16][j][0], qf[s16][j][1]);
+        for (int j = 0; j < NQT; ++j) {
+          uint32_t b0, b1;
+          if constexpr (Cfg::Q_SMEM) qfrag(s16, j, b0, b1);
+          else b0 = qreg[s16][j][0], b1 = qreg[s16][j][1];
+          mma16816<true>(S[j], A, b0, b1);
+        }
       }
     } else if constexpr (KK == KIND_NVFP4) {
       constexpr int RB = Cfg::K_RB;
@@ -354,8 +412,16 @@ __global__ void __launch_bounds__(128)
           const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
 #pragma unroll
           for (int j = 0; j < NQT; ++j) {
-            mma16816<false>(S[j], A0, qf[2 * cc][j][0], qf[2 * cc][j][1]);
-            mma16816<false>(S[j], A1, qf[2 * cc + 1][j][0], qf[2 * cc + 1][j][1]);
+            uint32_t b0, b1, c0, c1;
+            if constexpr (Cfg::Q_SMEM) {
+              qfrag(2 * cc, j, b0, b1);
+              qfrag(2 * cc + 1, j, c0, c1);
+            } else {
+              b0 = qreg[2 * cc][j][0], b1 = qreg[2 * cc][j][1];
+              c0 = qreg[2 * cc + 1][j][0], c1 = qreg[2 * cc + 1][j][1];
+            }
+            mma16816<false>(S[j], A0, b0, b1);
+            mma16816<false>(S[j], A1, c0, c1);
           }
         }
       }
@@ -383,8 +449,11 @@ __global__ void __launch_bounds__(128)
                                  cvt_pair<KK, true>(d[2 * u]), cvt_pair<KK, true>(d[2 * u + 1])};
 #pragma unroll
           for (int j = 0; j < NQT; ++j) {
-            if constexpr (KK == KIND_INT8) mma16816<false>(Sg[j], A, qf[cc][j][0], qf[cc][j][1]);
-            else mma16816<false>(S[j], A, qf[cc][j][0], qf[cc][j][1]);
+            uint32_t b0, b1;
+            if constexpr (Cfg::Q_SMEM) qfrag(cc, j, b0, b1);
+            else b0 = qreg[cc][j][0], b1 = qreg[cc][j][1];
+            if constexpr (KK == KIND_INT8) mma16816<false>(Sg[j], A, b0, b1);
+            else mma16816<false>(S[j], A, b0, b1);
           }
         }
         if constexpr (KK == KIND_INT8) {
@@ -415,205 +484,160 @@ __global__ void __launch_bounds__(128)
       }
     }
 
-    // ---------------- scores, masking, tile max ---------------------------
+    // ---------------- scores, masking, online softmax (this warp's keys) ---------------
     const int kg0 = key0 + kr0, kg1 = key0 + kr1;
+    float alpha[NQT][2];
+    bool rescale = false;
 #pragma unroll
     for (int j = 0; j < NQT; ++j) {
       S[j][0] = kg0 <= lim[j][0] ? S[j][0] * sc : -INFINITY;
       S[j][1] = kg0 <= lim[j][1] ? S[j][1] * sc : -INFINITY;
       S[j][2] = kg1 <= lim[j][0] ? S[j][2] * sc : -INFINITY;
       S[j][3] = kg1 <= lim[j][1] ? S[j][3] * sc : -INFINITY;
-      float v0 = fmaxf(S[j][0], S[j][2]), v1 = fmaxf(S[j][1], S[j][3]);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, off));
-        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, off));
-      }
-      if (r == 0) {
-        red_max[warp * R + 8 * j + 2 * c] = v0;
-        red_max[warp * R + 8 * j + 2 * c + 1] = v1;
-      }
-    }
-    __syncthreads();  // (1) tile maxima visible; stage of page i-1 free
-    if (s_flags[0]) {
-      aborted = true;
-      break;
-    }
-    if (tid == 0 && i >= 1 && issued < n) issue(issued++);
-
-    // ---------------- online softmax, P to shared memory ---------------------
-    float alpha[NQT][2];
-#pragma unroll
-    for (int j = 0; j < NQT; ++j)
+      float v[2] = {fmaxf(S[j][0], S[j][2]), fmaxf(S[j][1], S[j][3])};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int qr = 8 * j + 2 * c + u;
-        float mx = m_run[j][u];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_max[w * R + qr]);
-        const float mu = mx == -INFINITY ? 0.f : mx;
+        for (int off = 4; off < 32; off <<= 1) v[u] = fmaxf(v[u], __shfl_xor_sync(0xffffffffu, v[u], off));
+        const float mx2 = fmaxf(m_run[j][u], v[u]);
+        const float mu = mx2 == -INFINITY ? 0.f : mx2;
         alpha[j][u] = ex2(m_run[j][u] - mu);
-        m_run[j][u] = mx;
-        const float p_a = ex2(S[j][u] - mu), p_b = ex2(S[j][2 + u] - mu);
-        l_part[j][u] = l_part[j][u] * alpha[j][u] + p_a + p_b;
-        uint16_t ha, hb;
-        if constexpr (Cfg::MMA_BF16) {
-          const __nv_bfloat16 a_hi = __float2bfloat16_rn(p_a), b_hi = __float2bfloat16_rn(p_b);
-          ha = __bfloat16_as_ushort(a_hi);
-          hb = __bfloat16_as_ushort(b_hi);
-          const uint16_t la = __bfloat16_as_ushort(__float2bfloat16_rn(p_a - __bfloat162float(a_hi)));
-          const uint16_t lb = __bfloat16_as_ushort(__float2bfloat16_rn(p_b - __bfloat162float(b_hi)));
-          *reinterpret_cast<uint16_t*>(Ps + Cfg::P_BUF + qr * Cfg::P_PITCH + kr0 * 2) = la;
-          *reinterpret_cast<uint16_t*>(Ps + Cfg::P_BUF + qr * Cfg::P_PITCH + kr1 * 2) = lb;
-        } else {
-          ha = __half_as_ushort(__float2half_rn(p_a));
-          hb = __half_as_ushort(__float2half_rn(p_b));
-        }
-        *reinterpret_cast<uint16_t*>(Ps + qr * Cfg::P_PITCH + kr0 * 2) = ha;
-        *reinterpret_cast<uint16_t*>(Ps + qr * Cfg::P_PITCH + kr1 * 2) = hb;
+        rescale |= (mx2 != m_run[j][u]);
+        m_run[j][u] = mx2;
+        S[j][u] = ex2(S[j][u] - mu);
+        S[j][2 + u] = ex2(S[j][2 + u] - mu);
+        l_part[j][u] = l_part[j][u] * alpha[j][u] + S[j][u] + S[j][2 + u];
       }
-    __syncthreads();  // (2) P complete
-
-    // ---------------- PV: O^T(dims of this warp x R) += V^T P^T ---------------
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-    for (int mt = 0; mt < Cfg::MT; ++mt)
+      for (int mt = 0; mt < Cfg::MT; ++mt)
 #pragma unroll
-      for (int j = 0; j < NQT; ++j) {
-        o[mt][j][0] *= alpha[j][0];
-        o[mt][j][1] *= alpha[j][1];
-        o[mt][j][2] *= alpha[j][0];
-        o[mt][j][3] *= alpha[j][1];
-      }
-    // P^T fragments: pf[buffer][j][ks][0..1] (buffer 1 = low bf16 part)
-    uint32_t pf[Cfg::NPBUF][NQT][4][2];
-#pragma unroll
-    for (int pb = 0; pb < Cfg::NPBUF; ++pb)
-#pragma unroll
-      for (int j = 0; j < NQT; ++j)
-#pragma unroll
-        for (int kp = 0; kp < 2; ++kp) {
-          const int qrow = 8 * j + (lane & 7);
-          const int kcol = 32 * kp + 8 * ((lane >> 3) & 1) + 16 * (lane >> 4);
-          ldsm_x4(smem_u32(Ps + pb * Cfg::P_BUF + qrow * Cfg::P_PITCH + kcol * 2), pf[pb][j][2 * kp][0],
-                  pf[pb][j][2 * kp][1], pf[pb][j][2 * kp + 1][0], pf[pb][j][2 * kp + 1][1]);
+        for (int j = 0; j < NQT; ++j) {
+          o[mt][j][0] *= alpha[j][0];
+          o[mt][j][1] *= alpha[j][1];
+          o[mt][j][2] *= alpha[j][0];
+          o[mt][j][3] *= alpha[j][1];
         }
-    const int kvalid = F - key0;  // keys >= kvalid of this page are past the frontier
-    const int dw0 = warp * Cfg::DW;
+    }
+    // P^T as the B operand of PV, straight from registers: (key r, rows 2c,2c+1)
+    // transposed by movmatrix gives (row r, keys 2c, 2c+1).
+    uint32_t pb[Cfg::MMA_BF16 ? 2 : 1][NQT][2];
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      // validity masks of keys (2c, 2c+1) and (2c+8, 2c+9) of this k-step
-      uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-      if (kvalid < 64) {
-        const int k0 = 16 * ks + 2 * c;
-        mlo = (k0 < kvalid ? 0x0000FFFFu : 0u) | (k0 + 1 < kvalid ? 0xFFFF0000u : 0u);
-        mhi = (k0 + 8 < kvalid ? 0x0000FFFFu : 0u) | (k0 + 9 < kvalid ? 0xFFFF0000u : 0u);
-      }
-      if constexpr (KV == KIND_BF16) {
-#pragma unroll
-        for (int mt = 0; mt < Cfg::MT; ++mt) {
-          const int key = 16 * ks + (lane & 7) + ((lane >> 4) & 1) * 8;
-          const int col = (dw0 + 16 * mt + 8 * ((lane >> 3) & 1)) * 2;
-          const uint32_t addr = vbase + (col / 128) * (64 * 128) + swz<128>(key, col % 128);
-          uint32_t A[4];
-          ldsm_x4_t(addr, A[0], A[1], A[2], A[3]);
-          A[0] &= mlo;
-          A[1] &= mlo;
-          A[2] &= mhi;
-          A[3] &= mhi;
-#pragma unroll
-          for (int j = 0; j < NQT; ++j) {
-            mma16816<true>(o[mt][j], A, pf[0][j][ks][0], pf[0][j][ks][1]);
-            mma16816<true>(o[mt][j], A, pf[1][j][ks][0], pf[1][j][ks][1]);
-          }
-        }
+    for (int j = 0; j < NQT; ++j) {
+      if constexpr (Cfg::MMA_BF16) {
+        // bf16 P as hi + lo parts (about 16 significant bits)
+        const __nv_bfloat162 hi0 = __floats2bfloat162_rn(S[j][0], S[j][1]);
+        const __nv_bfloat162 hi1 = __floats2bfloat162_rn(S[j][2], S[j][3]);
+        const __nv_bfloat162 lo0 = __floats2bfloat162_rn(S[j][0] - __low2float(hi0), S[j][1] - __high2float(hi0));
+        const __nv_bfloat162 lo1 = __floats2bfloat162_rn(S[j][2] - __low2float(hi1), S[j][3] - __high2float(hi1));
+        pb[0][j][0] = movm_t(*reinterpret_cast<const uint32_t*>(&hi0));
+        pb[0][j][1] = movm_t(*reinterpret_cast<const uint32_t*>(&hi1));
+        pb[Cfg::MMA_BF16 ? 1 : 0][j][0] = movm_t(*reinterpret_cast<const uint32_t*>(&lo0));
+        pb[Cfg::MMA_BF16 ? 1 : 0][j][1] = movm_t(*reinterpret_cast<const uint32_t*>(&lo1));
       } else {
-        constexpr int RB = Cfg::V_RB;
-        constexpr int EPT = Cfg::EPT;
-        const int kk0 = 16 * ks + 2 * c;
-        const int keys[4] = {kk0, kk0 + 1, kk0 + 8, kk0 + 9};
-        const uint8_t* vs_tile = st + Cfg::OFF_VS;
+        pb[0][j][0] = movm_t(pack_f16x2(S[j][0], S[j][1]));
+        pb[0][j][1] = movm_t(pack_f16x2(S[j][2], S[j][3]));
+      }
+    }
+
+    // ---------------- PV: O^T(all dims x R) += V^T P^T over this warp's keys --------------
+    const int kvalid = F - key0;  // keys >= kvalid of this page are past the frontier
+    uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+    if (kvalid < 64) {
+      mlo = (kk0 < kvalid ? 0x0000FFFFu : 0u) | (kk0 + 1 < kvalid ? 0xFFFF0000u : 0u);
+      mhi = (kk0 + 8 < kvalid ? 0x0000FFFFu : 0u) | (kk0 + 9 < kvalid ? 0xFFFF0000u : 0u);
+    }
+    if constexpr (KV == KIND_BF16) {
 #pragma unroll
-        for (int p = 0; p < Cfg::MT / (EPT / 2); ++p) {  // groups of 8*EPT dims
-          const int dg = dw0 + 8 * EPT * p;
-          const int dthr = dg + EPT * r;  // first dim of this thread in the group
-          uint32_t pair_lo[EPT], pair_hi[EPT];
-          if constexpr (KV == KIND_NVFP4) {
-            // 4-bit codes: EPT dims = EPT/2 bytes per key
-            uint32_t f[4][EPT / 2];
+      for (int mt = 0; mt < Cfg::MT; ++mt) {
+        const int key = 16 * warp + (lane & 7) + ((lane >> 4) & 1) * 8;
+        const int col = (16 * mt + 8 * ((lane >> 3) & 1)) * 2;
+        const uint32_t addr = vbase + (col / 128) * (64 * 128) + swz<128>(key, col % 128);
+        uint32_t A[4];
+        ldsm_x4_t(addr, A[0], A[1], A[2], A[3]);
+        A[0] &= mlo;
+        A[1] &= mlo;
+        A[2] &= mhi;
+        A[3] &= mhi;
 #pragma unroll
-            for (int kx = 0; kx < 4; ++kx) {
-              const int colb = dthr / 2;
-              const uint8_t* rowp = reinterpret_cast<const uint8_t*>(st + Cfg::OFF_V) +
-                                    (colb / RB) * (64 * RB) + swz<RB>(keys[kx], colb % RB);
-              const uint32_t wv = EPT == 4 ? *reinterpret_cast<const uint16_t*>(rowp) : *rowp;
-              const __half sv = __ushort_as_half(static_cast<uint16_t>(
-                  e4m3x2_to_f16x2(vs_tile[keys[kx] * Cfg::VSB + dthr / 16]) & 0xFFFFu));
-              const uint32_t s2 = pack_h2(sv, sv);
-              f[kx][0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(wv), s2);
-              if constexpr (EPT == 4) f[kx][1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(wv), s2);
-            }
+        for (int j = 0; j < NQT; ++j) {
+          mma16816<true>(o[mt][j], A, pb[0][j][0], pb[0][j][1]);
+          mma16816<true>(o[mt][j], A, pb[Cfg::MMA_BF16 ? 1 : 0][j][0], pb[Cfg::MMA_BF16 ? 1 : 0][j][1]);
+        }
+      }
+    } else {
+      constexpr int RB = Cfg::V_RB;
+      const int keys[4] = {kk0, kk0 + 1, kk0 + 8, kk0 + 9};
+      const uint8_t* vs_tile = st + Cfg::OFF_VS;
+      const uint8_t* vtile = st + Cfg::OFF_V;
 #pragma unroll
-            for (int e2 = 0; e2 < EPT / 2; ++e2) {
-              pair_lo[2 * e2] = __byte_perm(f[0][e2], f[1][e2], 0x5410);
-              pair_lo[2 * e2 + 1] = __byte_perm(f[0][e2], f[1][e2], 0x7632);
-              pair_hi[2 * e2] = __byte_perm(f[2][e2], f[3][e2], 0x5410);
-              pair_hi[2 * e2 + 1] = __byte_perm(f[2][e2], f[3][e2], 0x7632);
-            }
+      for (int p = 0; p < D / 32; ++p) {  // groups of 32 dims = 2 m-tiles
+        const int dthr = 32 * p + 4 * r;  // first dim of this thread in the group
+        uint32_t pair_lo[4], pair_hi[4];
+        if constexpr (KV == KIND_NVFP4) {
+          uint32_t f[4][2];
+#pragma unroll
+          for (int kx = 0; kx < 4; ++kx) {
+            const int colb = dthr / 2;
+            const uint32_t wv = *reinterpret_cast<const uint16_t*>(vtile + (colb / RB) * (64 * RB) +
+                                                                   swz<RB>(keys[kx], colb % RB));
+            const __half sv = __ushort_as_half(static_cast<uint16_t>(
+                e4m3x2_to_f16x2(vs_tile[keys[kx] * Cfg::VSB + dthr / 16]) & 0xFFFFu));
+            const uint32_t s2 = pack_h2(sv, sv);
+            f[kx][0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(wv), s2);
+            f[kx][1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(wv), s2);
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            pair_lo[2 * e2] = __byte_perm(f[0][e2], f[1][e2], 0x5410);
+            pair_lo[2 * e2 + 1] = __byte_perm(f[0][e2], f[1][e2], 0x7632);
+            pair_hi[2 * e2] = __byte_perm(f[2][e2], f[3][e2], 0x5410);
+            pair_hi[2 * e2 + 1] = __byte_perm(f[2][e2], f[3][e2], 0x7632);
+          }
+        } else {
+          uint32_t wv[4];
+#pragma unroll
+          for (int kx = 0; kx < 4; ++kx)
+            wv[kx] = *reinterpret_cast<const uint32_t*>(vtile + (dthr / RB) * (64 * RB) +
+                                                        swz<RB>(keys[kx], dthr % RB));
+          uint32_t slo, shi;  // (s_key0, s_key1), (s_key8, s_key9) as f16x2
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
+          if constexpr (KV == KIND_INT8) {
+            const int grp = p >> 1;
+            slo = sp[keys[0] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[1] * (Cfg::VSB / 2) + grp]) << 16);
+            shi = sp[keys[2] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[3] * (Cfg::VSB / 2) + grp]) << 16);
           } else {
-            // 8-bit codes: EPT bytes per key
-            uint32_t wv[4];
+            slo = sp[keys[0]] | (uint32_t(sp[keys[1]]) << 16);
+            shi = sp[keys[2]] | (uint32_t(sp[keys[3]]) << 16);
+          }
 #pragma unroll
-            for (int kx = 0; kx < 4; ++kx) {
-              const uint8_t* rowp = reinterpret_cast<const uint8_t*>(st + Cfg::OFF_V) +
-                                    (dthr / RB) * (64 * RB) + swz<RB>(keys[kx], dthr % RB);
-              wv[kx] = EPT == 4 ? *reinterpret_cast<const uint32_t*>(rowp)
-                                : *reinterpret_cast<const uint16_t*>(rowp);
-            }
-            uint32_t slo, shi;  // (s_key0, s_key1), (s_key8, s_key9) as f16x2
+          for (int e = 0; e < 4; ++e) {
             if constexpr (KV == KIND_INT8) {
-              const int grp = dg / 64;
-              const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
-              slo = sp[keys[0] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[1] * (Cfg::VSB / 2) + grp]) << 16);
-              shi = sp[keys[2] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[3] * (Cfg::VSB / 2) + grp]) << 16);
+              const uint32_t sel = e | (e << 4) | ((4 + e) << 8) | ((4 + e) << 12);
+              pair_lo[e] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[0], wv[1], sel)), slo);
+              pair_hi[e] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[2], wv[3], sel)), shi);
             } else {
-              const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
-              slo = sp[keys[0]] | (uint32_t(sp[keys[1]]) << 16);
-              shi = sp[keys[2]] | (uint32_t(sp[keys[3]]) << 16);
-            }
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-              if constexpr (KV == KIND_INT8) {
-                const uint32_t sel = e | (e << 4) | ((4 + e) << 8) | ((4 + e) << 12);
-                pair_lo[e] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[0], wv[1], sel)), slo);
-                pair_hi[e] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[2], wv[3], sel)), shi);
-              } else {
-                const uint32_t sel = e | ((4 + e) << 4);
-                pair_lo[e] = hmul2_u32(e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(wv[0], wv[1], sel))), slo);
-                pair_hi[e] = hmul2_u32(e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(wv[2], wv[3], sel))), shi);
-              }
+              const uint32_t sel = e | ((4 + e) << 4);
+              pair_lo[e] = hmul2_u32(e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(wv[0], wv[1], sel))), slo);
+              pair_hi[e] = hmul2_u32(e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(wv[2], wv[3], sel))), shi);
             }
           }
+        }
 #pragma unroll
-          for (int mg = 0; mg < EPT / 2; ++mg) {
-            const uint32_t A[4] = {pair_lo[2 * mg] & mlo, pair_lo[2 * mg + 1] & mlo,
-                                   pair_hi[2 * mg] & mhi, pair_hi[2 * mg + 1] & mhi};
-            const int mt = p * (EPT / 2) + mg;
+        for (int mg = 0; mg < 2; ++mg) {
+          const uint32_t A[4] = {pair_lo[2 * mg] & mlo, pair_lo[2 * mg + 1] & mlo,
+                                 pair_hi[2 * mg] & mhi, pair_hi[2 * mg + 1] & mhi};
 #pragma unroll
-            for (int j = 0; j < NQT; ++j) mma16816<false>(o[mt][j], A, pf[0][j][ks][0], pf[0][j][ks][1]);
-          }
+          for (int j = 0; j < NQT; ++j) mma16816<false>(o[2 * p + mg][j], A, pb[0][j][0], pb[0][j][1]);
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 
-  if (aborted) {
-    if (tid == 0) {  // drain the copies still in flight (bounded)
-      for (int i = 0; i < issued; ++i) mbar_wait_bounded(&bars[i % NSTAGE], (i / NSTAGE) & 1, a.status, 100000000ull);
-    }
-    return;
-  }
-
-  // ---- final reductions of l over the 8 lanes of a column and the 4 warps ---
+  // ---- combine the four warps (fixed order), write partials or the output -----------
 #pragma unroll
   for (int j = 0; j < NQT; ++j)
 #pragma unroll
@@ -622,74 +646,86 @@ __global__ void __launch_bounds__(128)
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 16);
-      if (r == 0) red_l[warp * R + 8 * j + 2 * c + u] = v;
+      if (r == 0) {
+        red_m[warp * R + 8 * j + 2 * c + u] = m_run[j][u];
+        red_l[warp * R + 8 * j + 2 * c + u] = v;
+      }
     }
-  __syncthreads();
-  float l_tot[NQT][2];
+  if (aborted && lane == 0) s_flags[0] = 1;
+  consumer_sync();
+  if (s_flags[0]) {
+    // drain copies that may still be in flight, then leave without results
+    if (tid == 0)
+      for (int k = i; k < min(n, i + NSTAGE); ++k)
+        mbar_wait_bounded(&full[k % NSTAGE], (k / NSTAGE) & 1, a.status, 100000000ull);
+    return;
+  }
+  if (tid < R) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * R + tid]);
+    float Ls = 0.f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) Ls += red_l[w * R + tid] * ex2(red_m[w * R + tid] - M);
+    row_M[tid] = M;
+    row_L[tid] = Ls;
+  }
+  consumer_sync();
+  float* acc = reinterpret_cast<float*>(smem);  // [R][D], reuses the stage ring
+  float fac[NQT][2];
 #pragma unroll
   for (int j = 0; j < NQT; ++j)
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int qr = 8 * j + 2 * c + u;
-      l_tot[j][u] = red_l[qr] + red_l[R + qr] + red_l[2 * R + qr] + red_l[3 * R + qr];
+      const float M = row_M[8 * j + 2 * c + u];
+      fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
     }
-
+  for (int w = 0; w < 4; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < NQT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int qr = 8 * j + 2 * c + (e & 1), hi = e >> 1;
+            int d;
+            if constexpr (KV == KIND_BF16) d = 16 * mt + r + 8 * hi;
+            else d = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1) + hi;
+            const float v = o[mt][j][e] * fac[j][e & 1];
+            if (w == 0) acc[qr * D + d] = v;
+            else acc[qr * D + d] += v;
+          }
+    }
+    consumer_sync();
+  }
   const bool final_out = (nsplit == 1);
   const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + split;
-  const int dw0 = warp * Cfg::DW;
-#pragma unroll
-  for (int mt = 0; mt < Cfg::MT; ++mt)
-#pragma unroll
-    for (int j = 0; j < NQT; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int qr = 8 * j + 2 * c + (e & 1);
-        if (qr >= R_real) continue;
-        const int hi = e >> 1;
-        int d;
-        if constexpr (KV == KIND_BF16) {
-          d = dw0 + 16 * mt + r + 8 * hi;
-        } else {
-          constexpr int EPT = Cfg::EPT;
-          const int p = mt / (EPT / 2), mg = mt % (EPT / 2);
-          d = dw0 + 8 * EPT * p + EPT * r + 2 * mg + hi;
-        }
-        if (final_out) {
-          const float l = l_tot[j][e & 1];
-          const int t = qr / a.G, g = qr % a.G;
-          const int64_t oi = ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
-          a.out[oi] = __float2bfloat16_rn(l > 0.f ? o[mt][j][e] / l : 0.f);
-        } else {
-          a.ws_acc[(part * R + qr) * D + d] = o[mt][j][e];
-        }
+  for (int idx = tid; idx < R_real * D; idx += 128) {
+    const int qr = idx / D, d = idx % D;
+    if (final_out) {
+      const float L = row_L[qr];
+      const int t = qr / a.G, g = qr % a.G;
+      a.out[((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d] =
+          __float2bfloat16_rn(L > 0.f ? acc[idx] / L : 0.f);
+    } else {
+      a.ws_acc[(part * R + qr) * D + d] = acc[idx];
+    }
+  }
+  if (tid < R_real) {
+    if (final_out) {
+      if (a.lse) {
+        const int t = tid / a.G, g = tid % a.G;
+        const float L = row_L[tid];
+        a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
+            L > 0.f ? (row_M[tid] + log2f(L)) * kLn2 : -INFINITY;
       }
-  if (r == 0) {
-#pragma unroll
-    for (int j = 0; j < NQT; ++j)
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int qr = 8 * j + 2 * c + u;
-        if (qr >= R_real || warp != 0) continue;
-        if (final_out) {
-          if (a.lse) {
-            const int t = qr / a.G, g = qr % a.G;
-            const float l = l_tot[j][u];
-            a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
-                l > 0.f ? (m_run[j][u] + log2f(l)) * kLn2 : -INFINITY;
-          }
-        } else {
-          a.ws_ml[part * R + qr] = make_float2(m_run[j][u], l_tot[j][u]);
-        }
-      }
+    } else {
+      a.ws_ml[part * R + tid] = make_float2(row_M[tid], row_L[tid]);
+    }
   }
 }
-
-// Launch of one instantiation; returns a cudaError_t.
-struct DecodeLaunch {
-  int smem_bytes;
-  int nqt;
-  const void* kernel;
-};
 
 template <int KK, int KV, int D, int NQT>
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
@@ -702,7 +738,7 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k<<<grid, 128, Cfg::SMEM, s>>>(tk, tv, a);
+  k<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -714,7 +750,8 @@ int decode_ctas_per_sm() {
     auto k = decode_kernel<KK, KV, D, NQT>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, 128, Cfg::SMEM) != cudaSuccess || n < 1) n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, Cfg::THREADS, Cfg::SMEM) != cudaSuccess || n < 1)
+      n = 1;
     cached = n;
   }
   return cached;
