@@ -46,11 +46,19 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def make_workload(name):
+def make_workload(name, layers=None, context=None):
+    """The named workload; `layers` / `context` shrink it (profiling runs)."""
     from paged_kv_cache_append_gb300 import workloads as W
+    kw = {}
+    if layers:
+        kw["num_layers"] = layers
+    if context:
+        kw["S"] = context
     if name == "k8v4_verify":
-        return W.k8v4_long(T=4)
-    return W.WORKLOADS[name]()
+        return W.k8v4_long(T=4, **kw)
+    if name == "tiny_bf16":
+        return W.tiny_bf16()
+    return W.WORKLOADS[name](**kw)
 
 
 def workload_desc(w):
@@ -230,7 +238,7 @@ def run_gpu(args, rank, world):
     import torch
     device = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
     torch.cuda.set_device(device)
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.layers, args.context)
     hbm_peak, peak_kind = peaks()
     bench = Bench(w, device)
     flush, flush_bytes = _flush_fn(torch, device)
@@ -428,7 +436,7 @@ def cpu_baseline(w, seconds=15.0):
 
 
 def run_reference(args, rank, world):
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.layers, args.context)
     cores = len(os.sched_getaffinity(0))
     for _ in range(args.warmup):
         oracle_sample(w, [0])
@@ -463,6 +471,8 @@ def main():
     ap.add_argument("--impl", default="nk", choices=["nk", "reference"])
     ap.add_argument("--workload", default="int8_decode",
                     choices=["tiny_bf16", "int8_decode", "fp8_shared", "k8v4_long", "k8v4_verify"])
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling)")
+    ap.add_argument("--context", type=int, default=None, help="smaller max context S (profiling)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a, int R, int D) 
   __syncthreads();
   int total = 0;
   for (int bb = 0; bb < a.B; ++bb) total += (s_F[bb] + 63) >> 6;
-  const int chunk = max(1, (total + a.target - 1) / a.target);
+  const int chunk = split_chunk(total, a.target, a.B);
   const int ns = (((s_F[b] + 63) >> 6) + chunk - 1) / chunk;
   if (ns == 1) return;  // the decode CTA of this row wrote out / lse itself
   const int Rr = a.T * a.G;
@@ -183,7 +183,7 @@ extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_poo
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = launch_merge(a, pl.R, pool->desc.head_dim, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
@@ -243,7 +243,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
-  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target + B, a.H), s);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = launch_merge(a, pl.R, D, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

@@ -10,8 +10,9 @@
 // Work split.  A CTA owns one (row b, KV head h, page range).  The page
 // ranges come from the device-side frontiers, so the host needs no lengths and
 // the launch is graph-stable: with N_b = ceil(F_b / 64) pages, every CTA
-// computes chunk = ceil(sum_b N_b / target), row b gets ceil(N_b / chunk)
-// splits, and CTA x of a head takes the x-th split.
+// computes chunk = ceil(sum_b N_b / (target - B)), row b gets
+// ceil(N_b / chunk) splits (at most `target` in all: one wave), and CTA x of
+// a head takes the x-th split.
 //
 // Warp roles (160 threads).  Warp 4 is the producer: one lane stages page
 // tiles (K codes, V codes, K / V scales of one (page, head)) into a ring of
@@ -104,6 +105,10 @@ struct DecodeCfg {
   static constexpr int MISC_INTS = 32;
   static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
   static_assert(R * D * 4 <= NSTAGE * STAGE, "final combine reuses the stage ring");
+  // CTAs per SM the register allocation aims at: three (at most 136 registers
+  // a thread) when the O accumulators and register-resident q fragments fit in
+  // 64 registers, else two.
+  static constexpr int MINB = MT * NQT * 4 + (Q_SMEM ? 0 : KSTEPS * NQT * 2) > 64 ? 2 : 3;
 };
 
 // d index of the q element in slot i (0..3: b0.lo, b0.hi, b1.lo, b1.hi) of
@@ -123,6 +128,14 @@ __device__ __forceinline__ uint32_t cvt_pair(uint32_t w) {
   else return e4m3x2_to_f16x2(static_cast<uint16_t>(HI ? (w >> 16) : (w & 0xFFFFu)));
 }
 
+// Pages per split: with chunk = ceil(total / (target - B)) every row's
+// ceil(N_b / chunk) splits add up to at most `target` (one wave of CTAs).
+__host__ __device__ __forceinline__ int split_chunk(int total, int target, int B) {
+  const int t = target - B > 1 ? target - B : 1;
+  const int c = (total + t - 1) / t;
+  return c < 1 ? 1 : c;
+}
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -137,7 +150,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <int KK, int KV, int D, int NQT>
-__global__ void __launch_bounds__(160)
+__global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeArgs a) {
   using Cfg = DecodeCfg<KK, KV, D, NQT>;
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(160)
   // ---- which (row, split) this CTA owns --------------------------------------
   int total = 0;
   for (int bb = 0; bb < a.B; ++bb) total += (s_F[bb] + 63) >> 6;
-  const int chunk = max(1, (total + a.target - 1) / a.target);
+  const int chunk = split_chunk(total, a.target, a.B);
   int b = -1, split = 0, nsplit = 0, npages = 0;
   {
     int acc = 0;

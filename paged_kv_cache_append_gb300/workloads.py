@@ -146,11 +146,13 @@ def int8_decode(num_layers: int = 8, C: int = 8, S: int = 4096) -> Workload:
                     scale=1 / math.sqrt(256), seed=1002, outlier_p=0.01, outlier_mul=20.0)
 
 
-def fp8_shared(num_layers: int = 16, C: int = 8, S: int = 32768, shared_len: int = 16384,
+def fp8_shared(num_layers: int = 16, C: int = 8, S: int = 32768, shared_len: int | None = None,
                M: int | None = None) -> Workload:
+    """Shared prefix of S/2 tokens (16384 at S = 32768) unless given."""
+    if shared_len is None:
+        shared_len = S // 2
     L = -(-S // P)
     full = shared_len // P
-    has_tail = shared_len % P != 0
     if M is None:
         M = 2560 if (S, C) == (32768, 8) else full + C * (L - full) + 8
     rng = np.random.default_rng(3)
