@@ -1,5 +1,408 @@
-// prefill.cu -- chunked prefill / replay attention through the block tables.
+// prefill.cu -- chunked prefill / replay attention through the block tables on
+// the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+//
+// Contract: query i < chunk_len[b] of row b sits at logical position
+// prefix_len[b] + i and attends keys j <= prefix_len[b] + i of its table row
+// ("Paged KV cache" maintainer design page: pages are read in place through
+// the block table, a frontier may sit mid-page); the work is proportional to
+// the query-key pairs prefix * S + S (S + 1) / 2 ("Resource scheduling and
+// context cache" page, machine cost model).  BF16 pools.
+//
+// Tile.  A CTA owns 128 query rows of one (row b, KV head h): TQ = 128 / G
+// consecutive chunk tokens times the G query heads that share KV head h, so
+// every K / V page tile is loaded once for all of them.  Keys advance one page
+// (64 keys) at a time, which is also the P = 64 pipeline unit:
+//   S   = Q K^T   tcgen05.mma, M 128 x N 64 x K D, A = Q (shared, K-major,
+//                 128-byte swizzle), B = K page tile (shared, K-major), fp32
+//                 accumulator in TMEM (two buffers, ping-pong);
+//   P   = exp2(S * scale * log2 e - m) in bf16, written to TMEM by the four
+//                 softmax warps (one TMEM lane = one query row each);
+//   O  += P V     tcgen05.mma, M 128 x N D x K 64, A = P (TMEM), B = V page
+//                 tile (shared, MN-major), fp32 accumulator in TMEM.
+// The running max is rescaled lazily: O is rescaled only when the row max
+// grows by more than 2^8, so P stays below 256 and fp32 O never overflows.
+//
+// Warp roles (192 threads): warps 0-3 softmax and epilogue, warp 4 TMA
+// producer (Q once, then K and V page tiles through two rings), warp 5 the
+// single MMA-issuing thread.  All waits are bounded.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "internal.h"
+#include "tcgen05.cuh"
+
+namespace nk {
+
+struct PrefillArgs {
+  const int32_t* tables;
+  const int32_t* table_rows;
+  const int32_t* prefix_len;
+  const int32_t* chunk_len;
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  float scale_log2;  // softmax_scale * log2(e)
+  int B, Tc, Hq, H, G, L, M, C;
+};
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int THREADS = 192;
+  static constexpr int NK = D == 256 ? 2 : 3;  // K ring
+  static constexpr int NV = D == 256 ? 2 : 3;  // V ring
+  static constexpr int Q_BYTES = 128 * D * 2;  // 128 rows, D/64 column blocks of 16 KB
+  static constexpr int KV_BYTES = 64 * D * 2;  // one page tile, D/64 column blocks of 8 KB
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 64 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 256;
+  static constexpr uint32_t ID_S = tc::idesc_bf16(128, 64, false, false);
+  static constexpr uint32_t ID_O = tc::idesc_bf16(128, D, false, true);
+};
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, PrefillArgs a) {
+  using Cfg = PrefillCfg<D>;
+  constexpr int NK = Cfg::NK, NV = Cfg::NV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + Cfg::OFF_K;
+  uint8_t* sV = smem + Cfg::OFF_V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;   // [2]
+  uint64_t* s_empty = s_full + 2;    // [2]
+  uint64_t* p_full = s_empty + 2;    // [1]  (+1 spare)
+  uint64_t* o_done = p_full + 2;     // [1]  (+1 spare)
+  uint64_t* drain = o_done + 2;      // [1]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int G = a.G, TQ = 128 / G;
+
+  // ---- row geometry (uniform across the CTA) -------------------------------
+  const int row = a.table_rows[b];
+  int prefix = a.prefix_len[b], chunk = a.chunk_len[b];
+  if (row < 0 || row >= a.C || prefix < 0 || chunk < 0 || chunk > a.Tc ||
+      static_cast<int64_t>(prefix) + chunk > static_cast<int64_t>(a.L) * 64) {
+    if (tid == 0 && qt == 0 && h == 0) set_status(a.status, NK_STATUS_FRONTIER);
+    return;
+  }
+  const int t0 = qt * TQ;
+  if (t0 >= chunk) return;  // no query of this tile is in the chunk
+  const int t_last = min(t0 + TQ, chunk) - 1;
+  const int nkt = (prefix + t_last + 1 + 63) / 64;  // key pages to visit
+  const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmq);
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  if (warp == 0) {
+    tc::alloc(tslot, Cfg::TMEM_COLS);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 4) {
+    // ------------------------------ TMA producer ------------------------------
+    int gnext = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, Cfg::Q_BYTES);
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma_load_3d(sQ + kb * 16384, &tmq, kb * 64, h * G, b * a.Tc + t0, q_full);
+    }
+    for (int j = 0; j < nkt; ++j) {
+      if ((j & 31) == 0) gnext = (j + lane < nkt) ? table[j + lane] : 0;
+      int g = __shfl_sync(0xffffffffu, gnext, j & 31);
+      int stop = 0;
+      if (lane == 0) {
+        if (g < 0 || g >= a.M) {  // never copy from outside the pool
+          set_status(a.status, NK_STATUS_PAGE_RANGE);
+          g = 0;
+        }
+        const int y = (g * a.H + h) * 64;
+        const int ks = j % NK, vs = j % NV;
+        if (j >= NK && !mbar_wait_bounded(&k_empty[ks], ((j / NK) - 1) & 1, a.status)) stop = 1;
+        if (!stop) {
+          mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sK + ks * Cfg::KV_BYTES + kb * 8192, &tmk, kb * 128, y, &k_full[ks]);
+        }
+        if (!stop && j >= NV && !mbar_wait_bounded(&v_empty[vs], ((j / NV) - 1) & 1, a.status)) stop = 1;
+        if (!stop) {
+          mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sV + vs * Cfg::KV_BYTES + kb * 8192, &tmv, kb * 128, y, &v_full[vs]);
+        }
+        if (stop) *s_abort = 1;
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+    }
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      bool ok = mbar_wait_bounded(q_full, 0, a.status);
+      tc::fence_after();
+      const uint32_t qbase = smem_u32(sQ);
+      for (int j = 0; ok && j <= nkt; ++j) {
+        if (j < nkt) {
+          const int ks = j % NK, sb = j & 1;
+          ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status);
+          if (ok && j >= 2) ok = mbar_wait_bounded(&s_empty[sb], ((j / 2) - 1) & 1, a.status);
+          if (!ok) break;
+          tc::fence_after();
+          const uint32_t kbase = smem_u32(sK + ks * Cfg::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc(qbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = tc::smem_desc(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+            tc::mma_ss(tmem + Cfg::COL_S + 64 * sb, ad, bd, Cfg::ID_S, kk > 0);
+          }
+          tc::commit(&s_full[sb]);
+          tc::commit(&k_empty[ks]);
+        }
+        if (j >= 1) {  // O += P V for page j - 1
+          const int jj = j - 1, vs = jj % NV;
+          ok = mbar_wait_bounded(&v_full[vs], (jj / NV) & 1, a.status);
+          if (ok) ok = mbar_wait_bounded(p_full, jj & 1, a.status);
+          if (!ok) break;
+          tc::fence_after();
+          const uint32_t vbase = smem_u32(sV + vs * Cfg::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = tc::smem_desc(vbase + kk * 2048, 8192, 1024);
+            tc::mma_ts(tmem + Cfg::COL_O, tmem + Cfg::COL_P + kk * 8, bd, Cfg::ID_O, (jj > 0 || kk > 0));
+          }
+          tc::commit(o_done);
+          tc::commit(&v_empty[vs]);
+        }
+      }
+      if (!ok) *s_abort = 1;
+      tc::commit(drain);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ------------------------------ softmax warps -----------------------------
+    const int m = tid;  // query row = TMEM lane
+    const int tl = m / G, g = m % G;
+    const int token = t0 + tl;
+    const bool row_valid = token < chunk;
+    const int pos = prefix + token;  // keys <= pos are visible
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait_bounded(&s_full[sb], (j / 2) & 1, a.status) && !*s_abort;
+      if (!ok) break;
+      tc::fence_after();
+      uint32_t v0[32], v1[32];
+      tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb, v0);
+      tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb + 32, v1);
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(&s_empty[sb]);
+      // scores in base 2 with the causal mask at absolute positions
+      const int kmax = row_valid ? pos - 64 * j : -1;  // keys c <= kmax of this page are visible
+      float s[64];
+      float rmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = c <= kmax ? __uint_as_float(v0[c]) * a.scale_log2 : -INFINITY;
+        s[32 + c] = 32 + c <= kmax ? __uint_as_float(v1[c]) * a.scale_log2 : -INFINITY;
+        rmax = fmaxf(rmax, fmaxf(s[c], s[32 + c]));
+      }
+      float factor = 1.f;
+      const float mnew = fmaxf(m_used, rmax);
+      bool resc = false;
+      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + 8.f)) {
+        factor = m_used == -INFINITY ? 0.f : ex2(m_used - mnew);
+        m_used = mnew;
+        resc = true;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      uint32_t pk[32];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float pa = ex2(s[2 * c] - mu), pb = ex2(s[2 * c + 1] - mu);
+        sum += pa + pb;
+        pk[c] = pack_bf16x2(pa, pb);
+      }
+      l = l * factor + sum;
+      // P of page j may overwrite P of page j - 1 once O += P V for it is done
+      if (j >= 1) {
+        ok = mbar_wait_bounded(o_done, (j - 1) & 1, a.status) && !*s_abort;
+        if (!ok) break;
+      }
+      tc::fence_after();
+      if (__any_sync(0xffffffffu, resc && j >= 1)) {
+        const float f = (resc && j >= 1) ? factor : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tc::ld32(tmem + lane_base + Cfg::COL_O + c0, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
+          tc::st32(tmem + lane_base + Cfg::COL_O + c0, ov);
+        }
+      }
+      tc::st32(tmem + lane_base + Cfg::COL_P, pk);
+      tc::wait_st();
+      // Rows of the V page past the row's frontier hold stale bytes (possibly
+      // NaN); their P is 0, but 0 * NaN would still poison O, so zero them.
+      const int kstale = prefix + chunk - 64 * j;
+      if (kstale < 64) {
+        const int vs = j % NV;
+        ok = mbar_wait_bounded(&v_full[vs], (j / NV) & 1, a.status);
+        uint8_t* vt = sV + vs * Cfg::KV_BYTES;
+        const int nrow = 64 - kstale;
+        for (int i2 = tid; i2 < nrow * (D / 64) * 8; i2 += 128) {
+          const int rr = kstale + i2 / ((D / 64) * 8), rem = i2 % ((D / 64) * 8);
+          *reinterpret_cast<uint4*>(vt + (rem >> 3) * 8192 + rr * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!ok) break;
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(p_full);
+    }
+    // ---- epilogue: O / l to bf16 -------------------------------------------
+    if (ok) ok = mbar_wait_bounded(o_done, (nkt - 1) & 1, a.status) && !*s_abort;
+    tc::fence_after();
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tc::ld32(tmem + lane_base + Cfg::COL_O + c0, ov);
+        tc::wait_ld();
+        if (row_valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + c0 + 8 * c) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      if (row_valid && a.lse)
+        a.lse[(static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g] =
+            l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+
+  // ---- teardown: every issued MMA has completed before TMEM is freed ---------
+  if (warp < 4 && tid == 0) mbar_wait_bounded(drain, 0, a.status, 200000000ull);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 0) tc::dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+// 3-D TMA descriptor of q [B*Tc][Hq][D] (bf16): boxes of 64 dims x G heads x
+// TQ tokens = 128 rows of 128 bytes, swizzled like the K / V page tiles.
+static int encode_q_tmap(CUtensorMap* m, const void* q, int D, int Hq, int64_t rows, int G) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!fn) {
+      cudaDriverEntryPointQueryResult qr;
+      void* p = nullptr;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                       cudaEnableDefault, &qr);
+      if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !p)
+        return fail(NK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NK_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed with CUresult " + std::to_string(r));
+  return NK_OK;
+}
+
+template <int D>
+static cudaError_t launch_prefill(const CUtensorMap& tq, const nk_pool* p, int layer, const PrefillArgs& a,
+                                  dim3 grid, cudaStream_t s) {
+  using Cfg = PrefillCfg<D>;
+  auto k = prefill_kernel<D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tq, p->tmap[layer * 2 + 0], p->tmap[layer * 2 + 1], a);
+  return cudaGetLastError();
+}
+
+}  // namespace nk
 
 using namespace nk;
 
@@ -7,14 +410,58 @@ extern "C" int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_
                                           size_t* bytes) {
   clear_error();
   if (!pool || !bytes) return fail(NK_ERR_INVALID_ARG, "null argument");
-  *bytes = 0;
+  *bytes = 0;  // the tcgen05 prefill keeps everything in shared memory and TMEM
   return NK_OK;
 }
 
-extern "C" int nk_paged_prefill_attention(const void*, int32_t, const nk_pool*, int32_t,
-                                          const int32_t*, const int32_t*, const int32_t*,
-                                          const int32_t*, int32_t, int32_t, float, void*, float*,
-                                          void*, size_t, void*) {
+extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const nk_pool* pool,
+                                          int32_t layer, const int32_t* block_tables,
+                                          const int32_t* table_rows, const int32_t* prefix_len,
+                                          const int32_t* chunk_len, int32_t B, int32_t Tc,
+                                          float softmax_scale, void* out, float* lse,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  return fail(NK_ERR_UNSUPPORTED, "chunked prefill is not built yet");
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!q_chunk || !pool || !block_tables || !table_rows || !prefix_len || !chunk_len || !out)
+    return fail(NK_ERR_INVALID_ARG, "null argument to nk_paged_prefill_attention");
+  if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (pool->desc.profile != NK_BF16)
+    return fail(NK_ERR_UNSUPPORTED, "chunked prefill is built for BF16 pools");
+  const int D = pool->desc.head_dim, H = pool->desc.num_kv_heads;
+  if (D != 128 && D != 256) return fail(NK_ERR_UNSUPPORTED, "chunked prefill needs head_dim 128 or 256");
+  if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
+  if (B < 1 || B > pool->desc.max_concurrency) return fail(NK_ERR_SHAPE, "B must be in [1, C]");
+  if (Tc < 1) return fail(NK_ERR_SHAPE, "Tc must be >= 1");
+  if (Hq < 1 || Hq % H) return fail(NK_ERR_SHAPE, "Hq must be a positive multiple of num_kv_heads");
+  const int G = Hq / H;
+  if (G > 16 || 128 % G) return fail(NK_ERR_UNSUPPORTED, "GQA group must divide 128 and be <= 16");
+  if (!aligned16(q_chunk) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
+  CUtensorMap tq;
+  int rc = encode_q_tmap(&tq, q_chunk, D, Hq, static_cast<int64_t>(B) * Tc, G);
+  if (rc) return rc;
+  PrefillArgs a;
+  a.tables = block_tables;
+  a.table_rows = table_rows;
+  a.prefix_len = prefix_len;
+  a.chunk_len = chunk_len;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = pool->status;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.B = B;
+  a.Tc = Tc;
+  a.Hq = Hq;
+  a.H = H;
+  a.G = G;
+  a.L = pool->L;
+  a.M = pool->M;
+  a.C = pool->desc.max_concurrency;
+  const int TQ = 128 / G;
+  const dim3 grid((Tc + TQ - 1) / TQ, H, B);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 256 ? launch_prefill<256>(tq, pool, layer, a, grid, s)
+                           : launch_prefill<128>(tq, pool, layer, a, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return NK_OK;
 }

@@ -1,0 +1,96 @@
+"""GPU parity of the tcgen05 chunked prefill / replay attention against the
+oracle, through the C ABI.  The chunk's K/V are appended first; every query
+i < chunk_len[b] attends keys <= prefix_len[b] + i through the block table."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import formats as OF
+from paged_kv_cache_append_gb300 import workloads as W
+from paged_kv_cache_append_gb300.workloads import bf16_to_bits
+from tests.scenario import Scenario, compare_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_workload(Hkv, G, D, S, prefixes, chunks, Tc, seed, n_decode=0, layers=1):
+    rng = np.random.default_rng(seed)
+    C = len(prefixes) + n_decode
+    L = -(-S // 64)
+    M = C * L
+    tables = rng.permutation(M).astype(np.int32).reshape(C, L)
+    Bp = len(prefixes)
+    return W.Workload("prefill_test", "bf16", layers, Hkv * G, Hkv, D, S, C, M, tables,
+                      table_rows=np.arange(Bp, C, dtype=np.int32),
+                      context=np.full(n_decode, 10, np.int32),
+                      prefill_rows=np.arange(Bp, dtype=np.int32),
+                      prefix_len=np.asarray(prefixes, np.int32), chunk_len=np.asarray(chunks, np.int32),
+                      Tc=Tc, scale=1 / math.sqrt(D), seed=seed + 9000)
+
+
+def run_prefill(w, layer=0, poison=False, sample_rows=None):
+    sc = Scenario(w, layers=(layer,), oracle=True)
+    dev = "cuda"
+    k, v = w.chunk_kv(layer)
+    q = w.chunk_q(layer)
+    rows = torch.from_numpy(w.prefill_rows).to(dev)
+    pre = torch.from_numpy(w.prefix_len).to(dev)
+    chk = torch.from_numpy(w.chunk_len).to(dev)
+    sc.gpu.append(layer, sc.tables_d, rows, pre, k.to(dev), v.to(dev), counts=chk)
+    sc.orc.append(layer, w.tables, w.prefill_rows, w.prefix_len, bf16_to_bits(k), bf16_to_bits(v),
+                  counts=w.chunk_len)
+    if poison:  # bytes past each row's frontier in its last page: 0xFF (NaN bf16)
+        for i, r in enumerate(w.prefill_rows):
+            F = int(w.prefix_len[i] + w.chunk_len[i])
+            if F % 64 == 0:
+                continue
+            g = int(w.tables[r, F // 64])
+            for pi, plane in enumerate(sc.gpu.planes[layer]):
+                rb = sc.gpu.row_bytes[pi]
+                for hh in range(w.Hkv):
+                    base = ((g * w.Hkv + hh) * 64) * rb
+                    plane[base + (F % 64) * rb: base + 64 * rb] = 0xFF
+    out, lse = sc.gpu.prefill(layer, q.to(dev), sc.tables_d, rows, pre, chk, w.scale)
+    torch.cuda.synchronize()
+    out, lse = out.cpu(), lse.cpu()
+    qf = OF.bf16_bits_to_f64(bf16_to_bits(q))
+    for i, r in enumerate(w.prefill_rows):
+        P0, Cn = int(w.prefix_len[i]), int(w.chunk_len[i])
+        K, V = sc.orc.gather(layer, w.tables[r], P0 + Cn)
+        toks = np.arange(Cn) if sample_rows is None else np.unique(np.clip(sample_rows, 0, Cn - 1))
+        ref_o = np.zeros((len(toks), w.Hq, w.D))
+        ref_l = np.zeros((len(toks), w.Hq))
+        for n, t in enumerate(toks):
+            o1, l1 = OA.decode(qf[i, t:t + 1], K, V, P0 + t + 1, w.scale)
+            ref_o[n], ref_l[n] = o1[0], l1[0]
+        compare_attention(out[i, toks], lse[i, toks], ref_o, ref_l)
+        if Cn < w.Tc:   # rows past the chunk are not written
+            assert torch.all(out[i, Cn:] == 0) and torch.all(torch.isneginf(lse[i, Cn:]))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("G", [8, 1, 16])
+def test_prefill_small(D, G):
+    """Two rows: a mid-page prefix and a ragged chunk that spans several
+    128-row tiles (and one row with an empty prefix)."""
+    w = prefill_workload(2 if G < 16 else 1, G, D, 1024, prefixes=[133, 0], chunks=[300, 77], Tc=320,
+                         seed=D + G)
+    run_prefill(w)
+
+
+def test_prefill_stale_tail_is_not_read():
+    w = prefill_workload(2, 8, 256, 1024, prefixes=[100, 37], chunks=[45, 200], Tc=256, seed=5)
+    run_prefill(w, poison=True)
+
+
+def test_prefill_bf16_workload_sampled():
+    """The BF16 chunked-prefill workload at full size, one layer: 2 rows, a
+    2048-token chunk after a mid-page prefix of ~30.7k tokens, 16 q / 2 kv
+    heads, D 256; sampled query rows are checked against the oracle."""
+    w = W.bf16_prefill(num_layers=1)
+    sample = np.array([0, 1, 63, 64, 127, 128, 1000, 1023, 2046, 2047])
+    run_prefill(w, sample_rows=sample)
