@@ -46,6 +46,15 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def peaks_tensor():
+    """Dense bf16 tensor peak (burst: the prefill kernel is timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def make_workload(name, layers=None, context=None):
     """The named workload; `layers` / `context` shrink it (profiling runs)."""
     from paged_kv_cache_append_gb300 import workloads as W
@@ -163,6 +172,21 @@ class Bench:
         n = nk.nk_decode_workspace_bytes(self.pool.handle, B, w.T, w.Hq)
         self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
         self.launches_per_step = 3 * w.num_layers    # append + decode + merge per layer
+        # chunked prefill rows (bf16_prefill): append the chunk, then attend
+        self.Bp = len(w.prefill_rows) if share is None else 0
+        if self.Bp:
+            self.prow = torch.from_numpy(w.prefill_rows).to(device)
+            self.pre = torch.from_numpy(w.prefix_len).to(device)
+            self.chk = torch.from_numpy(w.chunk_len).to(device)
+            self.cq, self.ck, self.cv, self.cout = [], [], [], []
+            for layer in range(w.num_layers):
+                self.cq.append(w.chunk_q(layer, device=device).contiguous())
+                k, v = w.chunk_kv(layer, device=device)
+                self.ck.append(k.contiguous())
+                self.cv.append(v.contiguous())
+                self.cout.append(torch.empty_like(self.cq[-1]))
+            self.side = torch.cuda.Stream(device=device)
+            self.launches_per_step += 2 * w.num_layers   # chunk append + prefill per layer
 
     def _fill(self):
         """Context of every table row (device-side seeded values), written
@@ -172,6 +196,8 @@ class Bench:
         sh, full, tail = w.shared_len, w.shared_len // P, w.shared_len % P
         ctx = np.zeros(w.C, np.int64)
         ctx[w.table_rows] = w.context
+        if len(w.prefill_rows):
+            ctx[w.prefill_rows] = w.prefix_len
         gen_dev = self.dev if w.S * w.C * w.Hkv * w.D > (1 << 26) else "cpu"
         for layer in range(w.num_layers):
             for r in range(w.C):
@@ -195,11 +221,38 @@ class Bench:
 
     def step(self, stream=None):
         w = self.w
+        torch = self.torch
+        if self.Bp:   # prefill rows on a second stream, joined at the end of the step
+            cur = torch.cuda.current_stream()
+            self.side.wait_stream(cur)
+            with torch.cuda.stream(self.side):
+                for layer in range(w.num_layers):
+                    self.prefill_only(layer, append=True)
         for layer in range(w.num_layers):
             self.pool.append(layer, self.tables, self.rows, self.ctx, self.k[layer], self.v[layer],
                              stream=stream)
             self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
                              out=self.out[layer], lse=self.lse[layer], workspace=self.ws, stream=stream)
+
+        if self.Bp:
+            torch.cuda.current_stream().wait_stream(self.side)
+
+    def prefill_only(self, layer, append=False):
+        w = self.w
+        if append:
+            self.pool.append(layer, self.tables, self.prow, self.pre, self.ck[layer], self.cv[layer],
+                             counts=self.chk)
+        self.pool.prefill(layer, self.cq[layer], self.tables, self.prow, self.pre, self.chk, w.scale,
+                          out=self.cout[layer], lse=None)
+
+    def flops_prefill_layer(self):
+        """Algorithmic flops of one prefill launch: 4 * D * Hq * (prefix * S +
+        S (S + 1) / 2) per row (QK^T and PV over the visible query-key pairs)."""
+        w = self.w
+        tot = 0
+        for P0, S in zip(w.prefix_len.astype(np.int64), w.chunk_len.astype(np.int64)):
+            tot += 4 * w.D * w.Hq * (P0 * S + S * (S + 1) // 2)
+        return int(tot)
 
     def decode_only(self, layer):
         w = self.w
@@ -225,6 +278,8 @@ class Bench:
         return self.B * w.T * w.Hkv * (2 * w.D * 2 + self.pool.kv_bytes_per_token_head())
 
     def bytes_step(self):
+        """Decode-side algorithmic bytes of a step (the prefill rows are
+        reported in flops)."""
         return self.w.num_layers * (self.bytes_decode_layer() + self.bytes_append_layer())
 
 
@@ -294,24 +349,59 @@ def run_gpu(args, rank, world):
     kms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in kev)
     achieved = bench.bytes_decode_layer() / (kms * 1e-3) / 1e9
 
+    # ---- prefill kernel (bf16_prefill): tensor roofline ---------------------------
+    prefill_line = None
+    if bench.Bp:
+        tf_peak, tf_kind = peaks_tensor()
+        pev = []
+        for _ in range(max(3, args.steps // 4)):
+            for layer in range(w.num_layers):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush()
+                e0.record(stream)
+                bench.prefill_only(layer)
+                e1.record(stream)
+                pev.append((e0, e1))
+        torch.cuda.synchronize()
+        pms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in pev)
+        tflops = bench.flops_prefill_layer() / (pms * 1e-3) / 1e12
+        prefill_line = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tf_peak,
+                        "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": round(tflops / tf_peak, 4),
+                        "traffic": None, "kernel": "nk_paged_prefill_attention (tcgen05), one layer",
+                        "algorithmic_flops_per_launch": bench.flops_prefill_layer(),
+                        "avg_launch_ms": round(pms, 4)}
+
     # ---- end to end through the C ABI with host buffers ----------------------
     qh = [x.cpu().pin_memory() for x in bench.q]
     kh = [x.cpu().pin_memory() for x in bench.k]
     vh = [x.cpu().pin_memory() for x in bench.v]
     oh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bench.out]
     lh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bench.lse]
-    h2d = sum(x.numel() * x.element_size() for x in qh + kh + vh)
-    d2h = sum(x.numel() * x.element_size() for x in oh + lh)
+    if bench.Bp:
+        cqh = [x.cpu().pin_memory() for x in bench.cq]
+        ckh = [x.cpu().pin_memory() for x in bench.ck]
+        cvh = [x.cpu().pin_memory() for x in bench.cv]
+        coh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bench.cout]
+    else:
+        cqh = ckh = cvh = coh = []
+    h2d = sum(x.numel() * x.element_size() for x in qh + kh + vh + cqh + ckh + cvh)
+    d2h = sum(x.numel() * x.element_size() for x in oh + lh + coh)
 
     def e2e_step():
         for i in range(w.num_layers):
             bench.q[i].copy_(qh[i], non_blocking=True)
             bench.k[i].copy_(kh[i], non_blocking=True)
             bench.v[i].copy_(vh[i], non_blocking=True)
+            if bench.Bp:
+                bench.cq[i].copy_(cqh[i], non_blocking=True)
+                bench.ck[i].copy_(ckh[i], non_blocking=True)
+                bench.cv[i].copy_(cvh[i], non_blocking=True)
         graph.replay()
         for i in range(w.num_layers):
             oh[i].copy_(bench.out[i], non_blocking=True)
             lh[i].copy_(bench.lse[i], non_blocking=True)
+            if bench.Bp:
+                coh[i].copy_(bench.cout[i], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -390,6 +480,11 @@ def run_gpu(args, rank, world):
     }
     if sweep:
         line["sweep_rows_per_s"] = sweep
+    if prefill_line:
+        # the prefill kernel dominates this workload's step: it is the roofline
+        line["decode_roofline"] = line["roofline"]
+        line["roofline"] = prefill_line
+        line["prefill_tflops"] = prefill_line["achieved"]
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
@@ -470,7 +565,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="nk", choices=["nk", "reference"])
     ap.add_argument("--workload", default="int8_decode",
-                    choices=["tiny_bf16", "int8_decode", "fp8_shared", "k8v4_long", "k8v4_verify"])
+                    choices=["tiny_bf16", "int8_decode", "fp8_shared", "k8v4_long", "k8v4_verify",
+                             "bf16_prefill"])
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling)")
     ap.add_argument("--context", type=int, default=None, help="smaller max context S (profiling)")
     ap.add_argument("--no-sweep", action="store_true")
