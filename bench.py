@@ -170,8 +170,8 @@ class Bench:
         self.out = [torch.empty_like(x) for x in self.q]
         self.lse = [torch.empty((B, w.T, w.Hq), dtype=torch.float32, device=device) for _ in self.q]
         n = nk.nk_decode_workspace_bytes(self.pool.handle, B, w.T, w.Hq)
-        self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
-        self.launches_per_step = 3 * w.num_layers    # append + decode + merge per layer
+        self.ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+        self.launches_per_step = 2 * w.num_layers    # append + decode (merge in-kernel) per layer
         # chunked prefill rows (bf16_prefill): append the chunk, then attend
         self.Bp = len(w.prefill_rows) if share is None else 0
         if self.Bp:

@@ -176,9 +176,15 @@ int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t
  *   lse:  device fp32 [B][T][Hq] or NULL;  a row with F_b - T + t < 0 gets
  *         out = 0, lse = -inf.
  *   workspace: device scratch of at least nk_decode_workspace_bytes bytes
- *         (split-K partials; contents need no initialisation).
- * Split-K over pages with a log-sum-exp merge; no host synchronisation, so
- * the call can be captured in a CUDA graph (graph-stable arguments section).
+ *         holding the split-K partials and one counter per (row, KV head).
+ *         It must be zero-filled before its first use; every call leaves the
+ *         counters at zero again, so a workspace is zero-filled once and then
+ *         reused (two calls that share a workspace must not overlap).
+ * Split-K over pages with a log-sum-exp merge done by the last split of each
+ * (row, KV head) in the same launch; no host synchronisation, so the call can
+ * be captured in a CUDA graph (graph-stable arguments section).  Kernels are
+ * launched with programmatic stream serialization (they may start while the
+ * previous kernel in the stream drains, and read nothing before it completes).
  * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T*Hq/H > 64),
  * NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
 int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,

@@ -131,6 +131,8 @@ __device__ __forceinline__ void encode_row(const __nv_bfloat16* src, uint8_t* co
 
 template <int KK, int KV, int D>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  griddep_wait();  // launched with programmatic stream serialization
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (gw >= a.B * a.T * a.H) return;
@@ -166,9 +168,9 @@ template <int KK, int KV>
 static void launch_d(int D, const AppendArgs& a, cudaStream_t s) {
   const int warps = a.B * a.T * a.H;
   const dim3 grid((warps + 3) / 4), block(128);
-  if (D == 64) append_kernel<KK, KV, 64><<<grid, block, 0, s>>>(a);
-  else if (D == 128) append_kernel<KK, KV, 128><<<grid, block, 0, s>>>(a);
-  else append_kernel<KK, KV, 256><<<grid, block, 0, s>>>(a);
+  if (D == 64) launch_pdl(append_kernel<KK, KV, 64>, grid, block, 0, s, a);
+  else if (D == 128) launch_pdl(append_kernel<KK, KV, 128>, grid, block, 0, s, a);
+  else launch_pdl(append_kernel<KK, KV, 256>, grid, block, 0, s, a);
 }
 
 }  // namespace nk

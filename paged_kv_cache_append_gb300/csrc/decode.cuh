@@ -10,29 +10,32 @@
 // Work split.  A CTA owns one (row b, KV head h, page range).  The page
 // ranges come from the device-side frontiers, so the host needs no lengths and
 // the launch is graph-stable: with N_b = ceil(F_b / 64) pages, every CTA
-// computes chunk = ceil(sum_b N_b / (target - B)), row b gets
-// ceil(N_b / chunk) splits (at most `target` in all: one wave), and CTA x of
-// a head takes the x-th split.
+// computes chunk = max(ceil(sum_b N_b / (target - B)), ceil(max_b N_b / 16)),
+// row b gets ceil(N_b / chunk) splits (at most `target` in all: one wave; at
+// most 16 per row), and CTA x of a head takes the x-th split.
 //
-// Warp roles (160 threads).  Warp 4 is the producer: one lane stages page
-// tiles (K codes, V codes, K / V scales of one (page, head)) into a ring of
-// NSTAGE shared buffers with TMA / bulk copies, tracked by full / empty
-// mbarriers.  Warps 0..3 are consumers; consumer w owns keys [16w, 16w+16) of
-// every page and keeps its own online softmax, so the loop has no CTA-wide
+// Warp roles.  The last warp is the producer: one lane stages page tiles (K
+// codes, V codes, K / V scales of one (page, head)) into a ring of NSTAGE
+// shared buffers with TMA / bulk copies, tracked by full / empty mbarriers.
+// The consumers own 16-key slabs: slab p of every page is handled by one warp
+// (D <= 128), or at D = 256 by a pair of warps that each own half of the head
+// dims; a slab keeps its own online softmax, so the loop has no CTA-wide
 // barrier:
-//  QK:  S^T (16 keys x R query rows) by mma.m16n8k16 with the K tile as the A
-//       operand (ldmatrix of the raw codes, exact conversion to f16 / bf16 in
-//       registers) and q as B.  INT8-G64 group scales and FP8 row scales
-//       multiply the fp32 partial sums; NVFP4 scales multiply the f16 operand
-//       (exact product).
-//  softmax: base-2, running max per query row over the warp's keys.
-//  PV:  O^T (all D dims x R) += V^T P^T with P^T taken straight from the S
-//       registers by movmatrix, V^T built in registers from the V tile
+//  QK:  partial S^T (16 keys x R query rows) over the warp's dims by
+//       mma.m16n8k16 with the K tile as the A operand (ldmatrix of the raw
+//       codes, exact conversion to f16 / bf16 in registers) and q as B; the
+//       two halves are added through shared memory (same order in both
+//       warps).  INT8-G64 group scales and FP8 row scales multiply fp32
+//       partial sums; NVFP4 scales multiply the f16 operand (exact product).
+//  softmax: base-2, running max per query row over the pair's keys.
+//  PV:  O^T (the warp's dims x R) += V^T P^T with P^T taken straight from the
+//       S registers by movmatrix, V^T built in registers from the V tile
 //       (ldmatrix.trans for bf16; byte gathers for 8-bit and 4-bit codes), V
 //       scales folded in as f16 products.
-// At the end the four warps' (m, l, O) are combined in a fixed order, and the
+// At the end the four pairs' (m, l, O) are combined in a fixed order, and the
 // CTA writes unnormalised partials (m, l, acc) to the workspace, or the final
-// out / lse when its row has a single split.
+// out / lse when its row has a single split; the last split of a (row, head)
+// to finish merges them.
 #pragma once
 
 #include "device.cuh"
@@ -54,6 +57,7 @@ struct DecodeArgs {
   float* lse;
   float2* ws_ml;  // [B][H][maxsplit][R]
   float* ws_acc;  // [B][H][maxsplit][R][D]
+  int* counters;  // [B][H] splits finished; zero between calls (the last CTA resets it)
   int* status;
   float softmax_scale;
   int B, T, Hq, H, G, L, M, C;
@@ -75,7 +79,12 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int KK, int KV, int D, int NQT>
 struct DecodeCfg {
-  static constexpr int THREADS = 160;  // 4 consumer warps + 1 producer warp
+  // Head-dim split: at D = 256 the keys of a 16-key slab are shared by a pair
+  // of warps, each owning half of the dims (NH = 2); below, one warp per slab.
+  static constexpr int NH = D == 256 ? 2 : 1;
+  static constexpr int NW = 4 * NH;              // consumer warps
+  static constexpr int NCONS = 32 * NW;          // consumer threads
+  static constexpr int THREADS = NCONS + 32;     // + 1 producer warp
   static constexpr int R = 8 * NQT;    // query rows (T * G) padded to n-tiles of 8
   static constexpr int KCB = CodeRow<KK>::bytes(D);
   static constexpr int VCB = CodeRow<KV>::bytes(D);
@@ -94,22 +103,26 @@ struct DecodeCfg {
   // larger ones.
   static constexpr int NSTAGE = STAGE <= 16 * 1024 ? 4 : 2;
   static constexpr bool MMA_BF16 = (KK == KIND_BF16);
-  static constexpr int KSTEPS = D / 16;
-  static constexpr int MT = D / 16;  // m-tiles of PV (all head dims per warp)
-  // q fragments live in registers when they are few, else in shared memory
-  static constexpr bool Q_SMEM = KSTEPS * NQT * 2 > 32;
   static constexpr int Q_PITCH = D * 2 + 32;  // bytes per q row (padded against bank conflicts)
+  // q fragments of a warp live in registers when they are few, else they are
+  // read from shared memory (f16 / bf16 ready) at every k-step
+  static constexpr bool Q_SMEM = (D / NH / 16) * NQT * 2 > 32;
   static constexpr int OFF_Q = NSTAGE * STAGE;
-  static constexpr int OFF_RED = OFF_Q + align_up(R * Q_PITCH, 128);
-  static constexpr int OFF_BAR = OFF_RED + 4 * 4 * R * 4;  // m, l per warp; M, L per row
+  static constexpr int OFF_X = OFF_Q + align_up(R * Q_PITCH, 128);   // partial-S exchange [2][NW][32][NQT*4]
+  static constexpr int OFF_RED = OFF_X + (NH == 2 ? 2 * NW * 32 * NQT * 4 * 4 : 0);
+  static constexpr int OFF_BAR = OFF_RED + 10 * R * 4;  // m, l per pair; M, L per row
   static constexpr int MISC_INTS = 32;
   static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
   static_assert(R * D * 4 <= NSTAGE * STAGE, "final combine reuses the stage ring");
-  // CTAs per SM the register allocation aims at: three (at most 136 registers
-  // a thread) when the O accumulators and register-resident q fragments fit in
-  // 64 registers, else two.
-  static constexpr int MINB = MT * NQT * 4 + (Q_SMEM ? 0 : KSTEPS * NQT * 2) > 64 ? 2 : 3;
+  // CTAs per SM the register allocation aims at, from the O accumulators of
+  // a warp ((D / NH) x R fp32 over 32 lanes).
+  static constexpr int OREGS = (D / NH) * R / 32;
+  static constexpr int MINB = NH == 2 ? (OREGS > 32 ? 1 : 2) : (OREGS > 32 ? 2 : 3);
 };
+
+// At most this many splits per (row, KV head): bounds the merge work of the
+// last split.
+constexpr int kMaxSplits = 32;
 
 // d index of the q element in slot i (0..3: b0.lo, b0.hi, b1.lo, b1.hi) of
 // k-step s for lane column c; must match how the K operand is built.
@@ -142,37 +155,61 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   return y;
 }
 
-// Barrier of the four consumer warps only (named barrier 1).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the consumer warps only (named barrier 1).
+template <int NCONS>
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCONS) : "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 template <int KK, int KV, int D, int NQT>
-__global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
+__global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeCfg<KK, KV, D, NQT>::MINB))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeArgs a) {
   using Cfg = DecodeCfg<KK, KV, D, NQT>;
   constexpr int R = Cfg::R;
   constexpr int NSTAGE = Cfg::NSTAGE;
+  constexpr int NH = Cfg::NH, NW = Cfg::NW, NCONS = Cfg::NCONS;
+  constexpr int DH = D / NH;       // head dims of one consumer warp
+  constexpr int KSW = DH / 16;     // k-steps of QK per warp
+  constexpr int MTW = DH / 16;     // m-tiles of PV per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem + Cfg::OFF_Q;                                  // q rows [R][Q_PITCH]
+  float* sx = reinterpret_cast<float*>(smem + Cfg::OFF_X);         // [2][8][32][NQT*4] partial S
   float* red_m = reinterpret_cast<float*>(smem + Cfg::OFF_RED);    // [4][R]
   float* red_l = red_m + 4 * R;                                     // [4][R]
   float* row_M = red_l + 4 * R;                                     // [R]
   float* row_L = row_M + R;                                         // [R]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
-  int* s_flags = reinterpret_cast<int*>(empty + NSTAGE);  // [0] abort
-  int* s_F = s_flags + 4;                                 // [8] valid length per row
-  int* s_row = s_flags + 12;                              // [8] table row per row
-  float* s_qmax = reinterpret_cast<float*>(s_flags + 20); // [4] per-warp max|q|
+  int* s_flags = reinterpret_cast<int*>(empty + NSTAGE);    // [0] abort, [1] merging CTA
+  int* s_F = s_flags + 4;                                   // [8] valid length per row
+  int* s_row = s_flags + 12;                                // [8] table row per row
+  float* s_qmax = reinterpret_cast<float*>(s_flags + 20);   // [8] per-warp max|q|
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
+  // consumers: keys [16 pair, +16), dims [half DH, +DH)
+  const int pair = NH == 2 ? warp >> 1 : warp, half = NH == 2 ? warp & 1 : 0;
   const int h = blockIdx.y;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  // Launched with programmatic stream serialization: everything above overlaps
+  // the previous kernel's tail; nothing it wrote is read before this point.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // ---- per-row lengths, loaded once in parallel ------------------------------
   if (tid < a.B) {
@@ -182,22 +219,16 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     s_F[tid] = ok ? F : 0;
     s_row[tid] = ok ? row : 0;
   }
-  if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
-    }
-    s_flags[0] = 0;
-    fence_barrier_init();
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-  }
   __syncthreads();
 
   // ---- which (row, split) this CTA owns --------------------------------------
-  int total = 0;
-  for (int bb = 0; bb < a.B; ++bb) total += (s_F[bb] + 63) >> 6;
-  const int chunk = split_chunk(total, a.target, a.B);
+  int total = 0, maxp = 0;
+  for (int bb = 0; bb < a.B; ++bb) {
+    const int np = (s_F[bb] + 63) >> 6;
+    total += np;
+    maxp = max(maxp, np);
+  }
+  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
   int b = -1, split = 0, nsplit = 0, npages = 0;
   {
     int acc = 0;
@@ -221,7 +252,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
   const int R_real = a.T * a.G;
 
   // ---- producer warp: stage pages p0 .. p0+n-1 ---------------------------------
-  if (warp == 4) {
+  if (warp == NW) {
     const int32_t* table = a.tables + static_cast<int64_t>(s_row[b]) * a.L + p0;
     int gnext = 0;
     for (int i = 0; i < n; ++i) {
@@ -267,7 +298,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
   float mx = 0.f;
   {
     constexpr int V8 = D / 8;  // uint4 per row
-    for (int i = tid; i < R * V8; i += 128) {
+    for (int i = tid; i < R * V8; i += NCONS) {
       const int qr = i / V8, col = i % V8;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (qr < R_real) {
@@ -284,8 +315,9 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (lane == 0) s_qmax[warp] = mx;
   }
-  consumer_sync();
-  mx = fmaxf(fmaxf(s_qmax[0], s_qmax[1]), fmaxf(s_qmax[2], s_qmax[3]));
+  consumer_sync<NCONS>();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) mx = fmaxf(mx, s_qmax[w]);
   float qscale_log2 = 0.f, qf_mul = 1.f;
   if constexpr (!Cfg::MMA_BF16) {
     int ex = 0;
@@ -293,60 +325,68 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     const int e = mx > 0.f ? 15 - ex : 0;
     qf_mul = ldexpf(1.f, e);
     qscale_log2 = static_cast<float>(e);
-    if constexpr (Cfg::Q_SMEM) {  // convert in place to f16
-      for (int i = tid; i < R * D / 2; i += 128) {
-        const int qr = i / (D / 2), col = i % (D / 2);
-        uint32_t* p = reinterpret_cast<uint32_t*>(qs + qr * Cfg::Q_PITCH + col * 4);
-        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
-        *p = pack_f16x2(__low2float(v) * qf_mul, __high2float(v) * qf_mul);
-      }
-      consumer_sync();
-    }
   }
   const float sc = a.softmax_scale * kLog2e * exp2f(-qscale_log2);
 
-  // q fragment of k-step s, n-tile j: (b0, b1) read from shared memory
+  // q fragments of this warp's k-steps (global k-step half * KSW + s), in
+  // registers, or converted in place in shared memory when Q_SMEM
+  if constexpr (Cfg::Q_SMEM && !Cfg::MMA_BF16) {
+    for (int i2 = tid; i2 < R * D / 2; i2 += NCONS) {
+      const int qr = i2 / (D / 2), col = i2 % (D / 2);
+      uint32_t* p = reinterpret_cast<uint32_t*>(qs + qr * Cfg::Q_PITCH + col * 4);
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+      *p = pack_f16x2(__low2float(v) * qf_mul, __high2float(v) * qf_mul);
+    }
+    consumer_sync<NCONS>();
+  }
   auto qfrag = [&](int s, int j, uint32_t& b0, uint32_t& b1) {
     const uint8_t* row = qs + (8 * j + r) * Cfg::Q_PITCH;
+    const int sg = half * KSW + s;
     if constexpr (KK == KIND_BF16) {
-      b0 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(s, 0, c));
-      b1 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(s, 2, c));
+      b0 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(sg, 0, c));
+      b1 = *reinterpret_cast<const uint32_t*>(row + 2 * q_dim<KK>(sg, 2, c));
     } else {
-      const uint2 v = *reinterpret_cast<const uint2*>(row + 2 * q_dim<KK>(s, 0, c));
+      const uint2 v = *reinterpret_cast<const uint2*>(row + 2 * q_dim<KK>(sg, 0, c));
       b0 = v.x;
       b1 = v.y;
     }
   };
-  uint32_t qreg[Cfg::Q_SMEM ? 1 : Cfg::KSTEPS][Cfg::Q_SMEM ? 1 : NQT][2];
+  uint32_t qreg[Cfg::Q_SMEM ? 1 : KSW][Cfg::Q_SMEM ? 1 : NQT][2];
   if constexpr (!Cfg::Q_SMEM) {
 #pragma unroll
-    for (int s = 0; s < Cfg::KSTEPS; ++s)
+    for (int s = 0; s < KSW; ++s)
 #pragma unroll
       for (int j = 0; j < NQT; ++j) {
+        const uint8_t* row = qs + (8 * j + r) * Cfg::Q_PITCH;
+        const int sg = half * KSW + s;
         if constexpr (Cfg::MMA_BF16) {
           qfrag(s, j, qreg[s][j][0], qreg[s][j][1]);
         } else {
-          const uint8_t* row = qs + (8 * j + r) * Cfg::Q_PITCH;
           float v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(row + 2 * q_dim<KK>(s, i, c))) * qf_mul;
+            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(row + 2 * q_dim<KK>(sg, i, c))) * qf_mul;
           qreg[s][j][0] = pack_f16x2(v[0], v[1]);
           qreg[s][j][1] = pack_f16x2(v[2], v[3]);
         }
       }
   }
+  // B operand of k-step s, n-tile j
+  auto qb = [&](int s, int j, uint32_t& b0, uint32_t& b1) {
+    if constexpr (Cfg::Q_SMEM) qfrag(s, j, b0, b1);
+    else b0 = qreg[s][j][0], b1 = qreg[s][j][1];
+  };
 
   // ---- running state -----------------------------------------------------------
   float m_run[NQT][2], l_part[NQT][2];
-  float o[Cfg::MT][NQT][4];
+  float o[MTW][NQT][4];
 #pragma unroll
   for (int j = 0; j < NQT; ++j) {
     m_run[j][0] = m_run[j][1] = -INFINITY;
     l_part[j][0] = l_part[j][1] = 0.f;
   }
 #pragma unroll
-  for (int mt = 0; mt < Cfg::MT; ++mt)
+  for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
     for (int j = 0; j < NQT; ++j) o[mt][j][0] = o[mt][j][1] = o[mt][j][2] = o[mt][j][3] = 0.f;
 
@@ -357,9 +397,10 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
 #pragma unroll
     for (int u = 0; u < 2; ++u) lim[j][u] = min(F - a.T + (8 * j + 2 * c + u) / a.G, F - 1);
 
-  const int kr0 = 16 * warp + r, kr1 = kr0 + 8;                        // keys of this thread's S rows
-  const int krow_ld = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row of this lane
-  const int kk0 = 16 * warp + 2 * c;                                   // first PV key of this thread
+  const int kr0 = 16 * pair + r, kr1 = kr0 + 8;                        // keys of this thread's S rows
+  const int krow_ld = 16 * pair + (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row of this lane
+  const int kk0 = 16 * pair + 2 * c;                                   // first PV key of this thread
+  const uint32_t pair_bar = 2 + pair;                                  // named barrier of the warp pair
 
   bool aborted = false;
   int i = 0;
@@ -374,37 +415,38 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     }
     const int key0 = (p0 + i) * 64;
 
-    // ---------------- QK: S^T for this warp's 16 keys ------------------------------
+    // ---------------- QK: partial S^T over this warp's head dims ------------------
     float S[NQT][4];
 #pragma unroll
     for (int j = 0; j < NQT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+    const uint8_t* ks_tile = st + Cfg::OFF_KS;
     if constexpr (KK == KIND_BF16) {
 #pragma unroll
-      for (int s16 = 0; s16 < Cfg::KSTEPS; ++s16) {
-        const int col = (2 * s16 + (lane >> 4)) * 16;
+      for (int s16 = 0; s16 < KSW; ++s16) {
+        const int col = (2 * (half * KSW + s16) + (lane >> 4)) * 16;
         const uint32_t addr = kbase + (col / 128) * (64 * 128) + swz<128>(krow_ld, col % 128);
         uint32_t A[4];
         ldsm_x4(addr, A[0], A[1], A[2], A[3]);
 #pragma unroll
         for (int j = 0; j < NQT; ++j) {
           uint32_t b0, b1;
-          if constexpr (Cfg::Q_SMEM) qfrag(s16, j, b0, b1);
-          else b0 = qreg[s16][j][0], b1 = qreg[s16][j][1];
+          qb(s16, j, b0, b1);
           mma16816<true>(S[j], A, b0, b1);
         }
       }
     } else if constexpr (KK == KIND_NVFP4) {
       constexpr int RB = Cfg::K_RB;
-      const uint8_t* ks_tile = st + Cfg::OFF_KS;
+      constexpr int NCW = Cfg::KCB / 16 / NH;  // 16-byte chunks (32 dims) of this warp
 #pragma unroll
-      for (int cp = 0; cp < Cfg::KCB / 32; ++cp) {  // chunk pairs (64 dims)
-        const int col = (2 * cp + (lane >> 4)) * 16;
+      for (int cw = 0; cw < NCW; cw += 2) {
+        const int cc0 = half * NCW + cw;
+        const int col = (cc0 + (NCW > 1 ? (lane >> 4) : 0)) * 16;
         const uint32_t addr = kbase + (col / RB) * (64 * RB) + swz<RB>(krow_ld, col % RB);
         uint32_t d[4];
         ldsm_x4(addr, d[0], d[1], d[2], d[3]);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {  // chunk 2cp+u: regs d[2u] (key r), d[2u+1] (key r+8)
-          const int cc = 2 * cp + u;
+        for (int u = 0; u < (NCW > 1 ? 2 : 1); ++u) {  // chunk cc0+u: regs d[2u] (key r), d[2u+1] (key r+8)
+          const int cc = cc0 + u;
           const int blk = 2 * cc + (c >> 1);
           const __half s0 = __ushort_as_half(static_cast<uint16_t>(
               e4m3x2_to_f16x2(ks_tile[kr0 * Cfg::KSB + blk]) & 0xFFFFu));
@@ -412,27 +454,16 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
               e4m3x2_to_f16x2(ks_tile[kr1 * Cfg::KSB + blk]) & 0xFFFFu));
           const uint32_t sc0 = pack_h2(s0, s0), sc1 = pack_h2(s1, s1);
           const uint32_t w0 = d[2 * u], w1 = d[2 * u + 1];
-          uint32_t f0[4], f1[4];
-          f0[0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(w0), sc0);
-          f0[1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(w0), sc0);
-          f0[2] = hmul2_u32(e2m1x2_byte_to_f16x2<2>(w0), sc0);
-          f0[3] = hmul2_u32(e2m1x2_byte_to_f16x2<3>(w0), sc0);
-          f1[0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(w1), sc1);
-          f1[1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(w1), sc1);
-          f1[2] = hmul2_u32(e2m1x2_byte_to_f16x2<2>(w1), sc1);
-          f1[3] = hmul2_u32(e2m1x2_byte_to_f16x2<3>(w1), sc1);
-          const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
-          const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
+          const uint32_t A0[4] = {hmul2_u32(e2m1x2_byte_to_f16x2<0>(w0), sc0), hmul2_u32(e2m1x2_byte_to_f16x2<0>(w1), sc1),
+                                  hmul2_u32(e2m1x2_byte_to_f16x2<1>(w0), sc0), hmul2_u32(e2m1x2_byte_to_f16x2<1>(w1), sc1)};
+          const uint32_t A1[4] = {hmul2_u32(e2m1x2_byte_to_f16x2<2>(w0), sc0), hmul2_u32(e2m1x2_byte_to_f16x2<2>(w1), sc1),
+                                  hmul2_u32(e2m1x2_byte_to_f16x2<3>(w0), sc0), hmul2_u32(e2m1x2_byte_to_f16x2<3>(w1), sc1)};
+          const int sl = 2 * (cw + u);  // local k-steps of this chunk
 #pragma unroll
           for (int j = 0; j < NQT; ++j) {
             uint32_t b0, b1, c0, c1;
-            if constexpr (Cfg::Q_SMEM) {
-              qfrag(2 * cc, j, b0, b1);
-              qfrag(2 * cc + 1, j, c0, c1);
-            } else {
-              b0 = qreg[2 * cc][j][0], b1 = qreg[2 * cc][j][1];
-              c0 = qreg[2 * cc + 1][j][0], c1 = qreg[2 * cc + 1][j][1];
-            }
+            qb(sl, j, b0, b1);
+            qb(sl + 1, j, c0, c1);
             mma16816<false>(S[j], A0, b0, b1);
             mma16816<false>(S[j], A1, c0, c1);
           }
@@ -440,38 +471,36 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       }
     } else {  // INT8 / FP8: 16 dims per 16-byte chunk
       constexpr int RB = Cfg::K_RB;
-      constexpr int NCH = Cfg::KCB / 16;
-      const uint8_t* ks_tile = st + Cfg::OFF_KS;
+      constexpr int NCW = Cfg::KCB / 16 / NH;  // chunks of this warp (even)
+      constexpr bool LOCAL_GROUPS = (KK == KIND_INT8) && (DH >= 64);
       float Sg[NQT][4];
 #pragma unroll
-      for (int cp = 0; cp < NCH / 2; ++cp) {
-        if constexpr (KK == KIND_INT8) {
-          if ((cp & 1) == 0) {
+      for (int cw = 0; cw < NCW; cw += 2) {
+        if constexpr (LOCAL_GROUPS) {
+          if ((cw & 3) == 0) {
 #pragma unroll
             for (int j = 0; j < NQT; ++j) Sg[j][0] = Sg[j][1] = Sg[j][2] = Sg[j][3] = 0.f;
           }
         }
-        const int col = (2 * cp + (lane >> 4)) * 16;
+        const int col = (half * NCW + cw + (lane >> 4)) * 16;
         const uint32_t addr = kbase + (col / RB) * (64 * RB) + swz<RB>(krow_ld, col % RB);
         uint32_t d[4];
         ldsm_x4(addr, d[0], d[1], d[2], d[3]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int cc = 2 * cp + u;
           const uint32_t A[4] = {cvt_pair<KK, false>(d[2 * u]), cvt_pair<KK, false>(d[2 * u + 1]),
                                  cvt_pair<KK, true>(d[2 * u]), cvt_pair<KK, true>(d[2 * u + 1])};
 #pragma unroll
           for (int j = 0; j < NQT; ++j) {
             uint32_t b0, b1;
-            if constexpr (Cfg::Q_SMEM) qfrag(cc, j, b0, b1);
-            else b0 = qreg[cc][j][0], b1 = qreg[cc][j][1];
-            if constexpr (KK == KIND_INT8) mma16816<false>(Sg[j], A, b0, b1);
+            qb(cw + u, j, b0, b1);
+            if constexpr (LOCAL_GROUPS) mma16816<false>(Sg[j], A, b0, b1);
             else mma16816<false>(S[j], A, b0, b1);
           }
         }
-        if constexpr (KK == KIND_INT8) {
-          if ((cp & 1) == 1) {  // end of a 64-dim group: apply its scale
-            const int grp = cp >> 1;
+        if constexpr (LOCAL_GROUPS) {
+          if ((cw & 3) == 2) {  // end of a 64-dim group: apply its scale
+            const int grp = (half * NCW + cw) >> 2;
             const float g0 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr0 * Cfg::KSB + 2 * grp));
             const float g1 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr1 * Cfg::KSB + 2 * grp));
 #pragma unroll
@@ -484,20 +513,40 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
           }
         }
       }
-      if constexpr (KK == KIND_FP8) {
-        const float g0 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr0 * 2));
-        const float g1 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr1 * 2));
+    }
+
+    // ---------------- full S: add the partner warp's half (same order in both) ------
+    if constexpr (NH == 2) {
+      float* mine = sx + (((i & 1) * NW + warp) * 32 + lane) * (NQT * 4);
+      const float* other = sx + (((i & 1) * NW + (warp ^ 1)) * 32 + lane) * (NQT * 4);
 #pragma unroll
-        for (int j = 0; j < NQT; ++j) {
-          S[j][0] *= g0;
-          S[j][1] *= g0;
-          S[j][2] *= g1;
-          S[j][3] *= g1;
+      for (int j = 0; j < NQT; ++j)
+        *reinterpret_cast<float4*>(mine + 4 * j) = make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+#pragma unroll
+      for (int j = 0; j < NQT; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(other + 4 * j);
+        if (half == 0) {
+          S[j][0] += v.x; S[j][1] += v.y; S[j][2] += v.z; S[j][3] += v.w;
+        } else {
+          S[j][0] = v.x + S[j][0]; S[j][1] = v.y + S[j][1]; S[j][2] = v.z + S[j][2]; S[j][3] = v.w + S[j][3];
         }
       }
     }
+    if constexpr ((KK == KIND_INT8 && DH < 64) || KK == KIND_FP8) {
+      // FP8 row scale, or the single INT8 group shared by both halves
+      const float g0 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr0 * Cfg::KSB));
+      const float g1 = __half2float(*reinterpret_cast<const __half*>(ks_tile + kr1 * Cfg::KSB));
+#pragma unroll
+      for (int j = 0; j < NQT; ++j) {
+        S[j][0] *= g0;
+        S[j][1] *= g0;
+        S[j][2] *= g1;
+        S[j][3] *= g1;
+      }
+    }
 
-    // ---------------- scores, masking, online softmax (this warp's keys) ---------------
+    // ---------------- scores, masking, online softmax (this pair's keys) ---------------
     const int kg0 = key0 + kr0, kg1 = key0 + kr1;
     float alpha[NQT][2];
     bool rescale = false;
@@ -524,7 +573,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     }
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-      for (int mt = 0; mt < Cfg::MT; ++mt)
+      for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
         for (int j = 0; j < NQT; ++j) {
           o[mt][j][0] *= alpha[j][0];
@@ -554,7 +603,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       }
     }
 
-    // ---------------- PV: O^T(all dims x R) += V^T P^T over this warp's keys --------------
+    // ---------------- PV: O^T(this warp's dims x R) += V^T P^T over the pair's keys ------
     const int kvalid = F - key0;  // keys >= kvalid of this page are past the frontier
     uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
     if (kvalid < 64) {
@@ -563,9 +612,9 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     }
     if constexpr (KV == KIND_BF16) {
 #pragma unroll
-      for (int mt = 0; mt < Cfg::MT; ++mt) {
-        const int key = 16 * warp + (lane & 7) + ((lane >> 4) & 1) * 8;
-        const int col = (16 * mt + 8 * ((lane >> 3) & 1)) * 2;
+      for (int mt = 0; mt < MTW; ++mt) {
+        const int key = 16 * pair + (lane & 7) + ((lane >> 4) & 1) * 8;
+        const int col = (half * DH + 16 * mt + 8 * ((lane >> 3) & 1)) * 2;
         const uint32_t addr = vbase + (col / 128) * (64 * 128) + swz<128>(key, col % 128);
         uint32_t A[4];
         ldsm_x4_t(addr, A[0], A[1], A[2], A[3]);
@@ -585,8 +634,8 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       const uint8_t* vs_tile = st + Cfg::OFF_VS;
       const uint8_t* vtile = st + Cfg::OFF_V;
 #pragma unroll
-      for (int p = 0; p < D / 32; ++p) {  // groups of 32 dims = 2 m-tiles
-        const int dthr = 32 * p + 4 * r;  // first dim of this thread in the group
+      for (int p = 0; p < DH / 32; ++p) {  // groups of 32 dims = 2 m-tiles
+        const int dthr = half * DH + 32 * p + 4 * r;  // first dim of this thread in the group
         uint32_t pair_lo[4], pair_hi[4];
         if constexpr (KV == KIND_NVFP4) {
           uint32_t f[4][2];
@@ -617,7 +666,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
           uint32_t slo, shi;  // (s_key0, s_key1), (s_key8, s_key9) as f16x2
           const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
           if constexpr (KV == KIND_INT8) {
-            const int grp = p >> 1;
+            const int grp = dthr / 64;
             slo = sp[keys[0] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[1] * (Cfg::VSB / 2) + grp]) << 16);
             shi = sp[keys[2] * (Cfg::VSB / 2) + grp] | (uint32_t(sp[keys[3] * (Cfg::VSB / 2) + grp]) << 16);
           } else {
@@ -650,7 +699,8 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     if (lane == 0) mbar_arrive(&empty[s]);
   }
 
-  // ---- combine the four warps (fixed order), write partials or the output -----------
+  // ---- combine the four pairs (fixed order), write partials or the output -----------
+  // Both warps of a pair hold the same (m, l); each holds O for its own dims.
 #pragma unroll
   for (int j = 0; j < NQT; ++j)
 #pragma unroll
@@ -659,13 +709,13 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 16);
-      if (r == 0) {
-        red_m[warp * R + 8 * j + 2 * c + u] = m_run[j][u];
-        red_l[warp * R + 8 * j + 2 * c + u] = v;
+      if (r == 0 && half == 0) {
+        red_m[pair * R + 8 * j + 2 * c + u] = m_run[j][u];
+        red_l[pair * R + 8 * j + 2 * c + u] = v;
       }
     }
   if (aborted && lane == 0) s_flags[0] = 1;
-  consumer_sync();
+  consumer_sync<NCONS>();
   if (s_flags[0]) {
     // drain copies that may still be in flight, then leave without results
     if (tid == 0)
@@ -684,7 +734,7 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
     row_M[tid] = M;
     row_L[tid] = Ls;
   }
-  consumer_sync();
+  consumer_sync<NCONS>();
   float* acc = reinterpret_cast<float*>(smem);  // [R][D], reuses the stage ring
   float fac[NQT][2];
 #pragma unroll
@@ -695,27 +745,28 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
     }
   for (int w = 0; w < 4; ++w) {
-    if (warp == w) {
+    if (pair == w) {
 #pragma unroll
-      for (int mt = 0; mt < Cfg::MT; ++mt)
+      for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
         for (int j = 0; j < NQT; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int qr = 8 * j + 2 * c + (e & 1), hi = e >> 1;
             int d;
-            if constexpr (KV == KIND_BF16) d = 16 * mt + r + 8 * hi;
-            else d = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1) + hi;
+            if constexpr (KV == KIND_BF16) d = half * DH + 16 * mt + r + 8 * hi;
+            else d = half * DH + 32 * (mt >> 1) + 4 * r + 2 * (mt & 1) + hi;
             const float v = o[mt][j][e] * fac[j][e & 1];
             if (w == 0) acc[qr * D + d] = v;
             else acc[qr * D + d] += v;
           }
     }
-    consumer_sync();
+    consumer_sync<NCONS>();
   }
   const bool final_out = (nsplit == 1);
-  const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + split;
-  for (int idx = tid; idx < R_real * D; idx += 128) {
+  const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
+  const int64_t part = part0 + split;
+  for (int idx = tid; idx < R_real * D; idx += NCONS) {
     const int qr = idx / D, d = idx % D;
     if (final_out) {
       const float L = row_L[qr];
@@ -738,6 +789,70 @@ __global__ void __launch_bounds__(160, (DecodeCfg<KK, KV, D, NQT>::MINB))
       a.ws_ml[part * R + tid] = make_float2(row_M[tid], row_L[tid]);
     }
   }
+  if (final_out) return;
+
+  // ---- log-sum-exp merge by the last split of this (row, head) to finish ------
+  // Split s holds (m_s, l_s, acc_s); M = max_s m_s, L = sum_s l_s 2^(m_s - M),
+  // out = sum_s acc_s 2^(m_s - M) / L, lse = (M + log2 L) ln 2: the softmax over
+  // the union of the splits' keys.  Partials are published with a device-scope
+  // fence before the counter increment; the last CTA reads them from L2.
+  __threadfence();
+  consumer_sync<NCONS>();
+  if (tid == 0) {
+    const int done = atomicAdd(&a.counters[b * a.H + h], 1);
+    s_flags[1] = (done == nsplit - 1);
+  }
+  consumer_sync<NCONS>();
+  if (!s_flags[1]) return;
+  __threadfence();
+  float* wgt = acc + R * D;  // [R_real][nsplit] merge weights, in the stage ring
+  for (int qr = warp; qr < R_real; qr += NW) {
+    float M = -INFINITY;
+    for (int k = lane; k < nsplit; k += 32) M = fmaxf(M, __ldcg(&a.ws_ml[(part0 + k) * R + qr]).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float Ls = 0.f;
+    if (M != -INFINITY)
+      for (int k = lane; k < nsplit; k += 32) {
+        const float2 ml = __ldcg(&a.ws_ml[(part0 + k) * R + qr]);
+        Ls += ml.y * ex2(ml.x - M);
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    for (int k = lane; k < nsplit; k += 32)
+      wgt[qr * nsplit + k] = Ls > 0.f ? ex2(__ldcg(&a.ws_ml[(part0 + k) * R + qr]).x - M) * inv : 0.f;
+    if (lane == 0 && a.lse) {
+      const int t = qr / a.G, g = qr % a.G;
+      a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
+          Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    }
+  }
+  consumer_sync<NCONS>();
+  // four consecutive dims per thread (16-byte loads), splits unrolled by four
+  for (int idx = tid; idx < R_real * (D / 4); idx += NCONS) {
+    const int qr = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (part0 * R + qr) * D + d);
+    const int64_t stride = static_cast<int64_t>(R) * D / 4;
+    const float* w = wgt + qr * nsplit;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    int k = 0;
+    for (; k + 2 <= nsplit; k += 2) {
+      const float4 v0 = __ldcg(src + k * stride), v1 = __ldcg(src + (k + 1) * stride);
+      const float w0 = w[k], w1 = w[k + 1];
+      s0.x = fmaf(w0, v0.x, s0.x); s0.y = fmaf(w0, v0.y, s0.y); s0.z = fmaf(w0, v0.z, s0.z); s0.w = fmaf(w0, v0.w, s0.w);
+      s1.x = fmaf(w1, v1.x, s1.x); s1.y = fmaf(w1, v1.y, s1.y); s1.z = fmaf(w1, v1.z, s1.z); s1.w = fmaf(w1, v1.w, s1.w);
+    }
+    if (k < nsplit) {
+      const float4 v0 = __ldcg(src + k * stride);
+      const float w0 = w[k];
+      s0.x = fmaf(w0, v0.x, s0.x); s0.y = fmaf(w0, v0.y, s0.y); s0.z = fmaf(w0, v0.z, s0.z); s0.w = fmaf(w0, v0.w, s0.w);
+    }
+    const int t = qr / a.G, g = qr % a.G;
+    __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(s0.x + s1.x, s0.y + s1.y), pack_bf16x2(s0.z + s1.z, s0.w + s1.w));
+  }
+  if (tid == 0) a.counters[b * a.H + h] = 0;  // ready for the next call
 }
 
 template <int KK, int KV, int D, int NQT>
@@ -751,8 +866,14 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, tk, tv, a);
+}
+
+// Bytes of the stage ring, which the final combine and the merge reuse.
+template <int KK, int KV, int D, int NQT>
+int decode_ring_bytes() {
+  using Cfg = DecodeCfg<KK, KV, D, NQT>;
+  return Cfg::NSTAGE * Cfg::STAGE;
 }
 
 template <int KK, int KV, int D, int NQT>
@@ -773,7 +894,7 @@ int decode_ctas_per_sm() {
 // Per-profile entry points (defined in decode_<profile>.cu).
 using DecodeFn = cudaError_t (*)(const nk_pool*, int layer, const DecodeArgs&, int nqt, dim3 grid,
                                  cudaStream_t);
-using OccFn = int (*)(int D, int nqt);
+using OccFn = int (*)(int D, int nqt, int* ring_bytes);
 
 template <int KK, int KV>
 cudaError_t decode_dispatch(const nk_pool* p, int layer, const DecodeArgs& a, int nqt, dim3 grid,
@@ -791,13 +912,17 @@ cudaError_t decode_dispatch(const nk_pool* p, int layer, const DecodeArgs& a, in
 }
 
 template <int KK, int KV>
-int decode_occupancy(int D, int nqt) {
-#define NK_CASE(DD, Q) \
-  if (D == DD && nqt == Q) return decode_ctas_per_sm<KK, KV, DD, Q>();
+int decode_occupancy(int D, int nqt, int* ring_bytes) {
+#define NK_CASE(DD, Q)                                     \
+  if (D == DD && nqt == Q) {                               \
+    *ring_bytes = decode_ring_bytes<KK, KV, DD, Q>();      \
+    return decode_ctas_per_sm<KK, KV, DD, Q>();            \
+  }
   NK_CASE(64, 1) NK_CASE(64, 2) NK_CASE(64, 4)
   NK_CASE(128, 1) NK_CASE(128, 2) NK_CASE(128, 4)
   NK_CASE(256, 1) NK_CASE(256, 2)
 #undef NK_CASE
+  *ring_bytes = 0;
   return 1;
 }
 
@@ -806,10 +931,10 @@ cudaError_t decode_int8(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaS
 cudaError_t decode_fp8(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
 cudaError_t decode_nvfp4(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
 cudaError_t decode_k8v4(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
-int occupancy_bf16(int, int);
-int occupancy_int8(int, int);
-int occupancy_fp8(int, int);
-int occupancy_nvfp4(int, int);
-int occupancy_k8v4(int, int);
+int occupancy_bf16(int, int, int*);
+int occupancy_int8(int, int, int*);
+int occupancy_fp8(int, int, int*);
+int occupancy_nvfp4(int, int, int*);
+int occupancy_k8v4(int, int, int*);
 
 }  // namespace nk

@@ -8,6 +8,6 @@ cudaError_t decode_bf16(const nk_pool* p, int layer, const DecodeArgs& a, int nq
   return decode_dispatch<KIND_BF16, KIND_BF16>(p, layer, a, nqt, grid, s);
 }
 
-int occupancy_bf16(int D, int nqt) { return decode_occupancy<KIND_BF16, KIND_BF16>(D, nqt); }
+int occupancy_bf16(int D, int nqt, int* ring_bytes) { return decode_occupancy<KIND_BF16, KIND_BF16>(D, nqt, ring_bytes); }
 
 }  // namespace nk

@@ -8,6 +8,6 @@ cudaError_t decode_fp8(const nk_pool* p, int layer, const DecodeArgs& a, int nqt
   return decode_dispatch<KIND_FP8, KIND_FP8>(p, layer, a, nqt, grid, s);
 }
 
-int occupancy_fp8(int D, int nqt) { return decode_occupancy<KIND_FP8, KIND_FP8>(D, nqt); }
+int occupancy_fp8(int D, int nqt, int* ring_bytes) { return decode_occupancy<KIND_FP8, KIND_FP8>(D, nqt, ring_bytes); }
 
 }  // namespace nk

@@ -8,6 +8,6 @@ cudaError_t decode_int8(const nk_pool* p, int layer, const DecodeArgs& a, int nq
   return decode_dispatch<KIND_INT8, KIND_INT8>(p, layer, a, nqt, grid, s);
 }
 
-int occupancy_int8(int D, int nqt) { return decode_occupancy<KIND_INT8, KIND_INT8>(D, nqt); }
+int occupancy_int8(int D, int nqt, int* ring_bytes) { return decode_occupancy<KIND_INT8, KIND_INT8>(D, nqt, ring_bytes); }
 
 }  // namespace nk

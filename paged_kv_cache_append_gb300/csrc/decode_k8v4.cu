@@ -8,6 +8,6 @@ cudaError_t decode_k8v4(const nk_pool* p, int layer, const DecodeArgs& a, int nq
   return decode_dispatch<KIND_FP8, KIND_NVFP4>(p, layer, a, nqt, grid, s);
 }
 
-int occupancy_k8v4(int D, int nqt) { return decode_occupancy<KIND_FP8, KIND_NVFP4>(D, nqt); }
+int occupancy_k8v4(int D, int nqt, int* ring_bytes) { return decode_occupancy<KIND_FP8, KIND_NVFP4>(D, nqt, ring_bytes); }
 
 }  // namespace nk

@@ -8,6 +8,6 @@ cudaError_t decode_nvfp4(const nk_pool* p, int layer, const DecodeArgs& a, int n
   return decode_dispatch<KIND_NVFP4, KIND_NVFP4>(p, layer, a, nqt, grid, s);
 }
 
-int occupancy_nvfp4(int D, int nqt) { return decode_occupancy<KIND_NVFP4, KIND_NVFP4>(D, nqt); }
+int occupancy_nvfp4(int D, int nqt, int* ring_bytes) { return decode_occupancy<KIND_NVFP4, KIND_NVFP4>(D, nqt, ring_bytes); }
 
 }  // namespace nk

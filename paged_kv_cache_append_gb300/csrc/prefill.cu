@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(192, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, TQ = 128 / G;
+  griddep_wait();  // launched with programmatic stream serialization
+  griddep_launch_dependents();
 
   // ---- row geometry (uniform across the CTA) -------------------------------
   const int row = a.table_rows[b];
@@ -398,8 +400,8 @@ static cudaError_t launch_prefill(const CUtensorMap& tq, const nk_pool* p, int l
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k<<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(tq, p->tmap[layer * 2 + 0], p->tmap[layer * 2 + 1], a);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, tq, p->tmap[layer * 2 + 0],
+                    p->tmap[layer * 2 + 1], a);
 }
 
 }  // namespace nk

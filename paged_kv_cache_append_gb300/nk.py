@@ -225,8 +225,8 @@ class Pool:
     def workspace(self, B, T, Hq):
         import torch
         n = nk_decode_workspace_bytes(self.handle, B, T, Hq)
-        if self._ws is None or self._ws.numel() < n:
-            self._ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.planes[0][0].device)
+        if self._ws is None or self._ws.numel() < n:   # zero-filled once (split counters)
+            self._ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.planes[0][0].device)
         return self._ws
 
     def decode(self, layer, q, tables, table_rows, frontiers, scale, out=None, lse=None,
