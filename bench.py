@@ -55,6 +55,31 @@ def peaks_tensor():
     return 1900.0, "fallback"
 
 
+def traffic(workload, kernel, algorithmic_now):
+    """DRAM bytes per launch of the roofline kernel from the committed ncu
+    capture (profiles/traffic.json), scaled by algorithmic work to this
+    launch; None when the kernel's sources changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        ent = json.load(open(p))["workloads"][workload]
+    except (OSError, KeyError, ValueError):
+        return None
+    if ent.get("kernel") != kernel:
+        return None
+    h = hashlib.sha256()
+    for f in ent["files"]:
+        h.update(f.encode())
+        h.update(b"\0")
+        try:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        except OSError:
+            return None
+    if h.hexdigest() != ent["sha256"]:
+        return None
+    return int(round(ent["dram_bytes_per_launch"] * algorithmic_now / ent["algorithmic_per_launch_at_capture"]))
+
+
 def make_workload(name, layers=None, context=None):
     """The named workload; `layers` / `context` shrink it (profiling runs)."""
     from paged_kv_cache_append_gb300 import workloads as W
@@ -367,7 +392,10 @@ def run_gpu(args, rank, world):
         tflops = bench.flops_prefill_layer() / (pms * 1e-3) / 1e12
         prefill_line = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tf_peak,
                         "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": round(tflops / tf_peak, 4),
-                        "traffic": None, "kernel": "nk_paged_prefill_attention (tcgen05), one layer",
+                        "traffic": traffic(args.workload, "nk_paged_prefill_attention",
+                                           bench.flops_prefill_layer()),
+                        "traffic_unit": "bytes per launch",
+                        "kernel": "nk_paged_prefill_attention (tcgen05), one layer",
                         "algorithmic_flops_per_launch": bench.flops_prefill_layer(),
                         "avg_launch_ms": round(pms, 4)}
 
@@ -469,7 +497,10 @@ def run_gpu(args, rank, world):
         "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": None, "kernel": "nk_paged_decode_attention (decode + merge), one layer",
+                     "traffic": (traffic(args.workload, "nk_paged_decode_attention", bench.bytes_decode_layer())
+                                 if not bench.Bp else None),
+                     "traffic_unit": "bytes per launch",
+                     "kernel": "nk_paged_decode_attention (decode + merge), one layer",
                      "algorithmic_bytes_per_launch": bench.bytes_decode_layer(),
                      "avg_launch_ms": round(kms, 5)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -516,18 +547,26 @@ def oracle_sample(w, rows, layer=0):
 
 
 def cpu_baseline(w, seconds=15.0):
+    """The oracle on (layer, row) units of the workload, layer by layer,
+    until `seconds` have passed (at least one unit)."""
     cores = len(os.sched_getaffinity(0))
     t0 = time.perf_counter()
-    done, rows = 0, []
-    b = 0
-    while time.perf_counter() - t0 < seconds and b < w.B:
-        done += oracle_sample(w, [b])
-        rows.append(b)
-        b += 1
+    done, units = 0, 0
+    layer = 0
+    while True:
+        for b in range(w.B):
+            done += oracle_sample(w, [b], layer=layer % w.num_layers)
+            units += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        if time.perf_counter() - t0 >= seconds:
+            break
+        layer += 1
     dt = time.perf_counter() - t0
     return {"value": round(done / dt / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"layer 0, rows {rows} of {w.name}: encode context + step token, gather, "
-                      f"float64 attention ({dt:.1f} s)"}
+            "sample": f"{units} (layer, row) decode units of {w.name} ({units / w.B:.1f} layers of "
+                      f"{w.num_layers}; layers repeat past the last): encode context + step token, "
+                      f"gather, float64 attention, {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
