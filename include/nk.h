@@ -208,8 +208,10 @@ int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, in
  * (row, KV head) is rejected with NK_ERR_WORKSPACE before any launch.
  * The first call on a device (with that device current, which must be the
  * pool's device) looks up the array's device address; make it before any
- * stream capture.  All calls share the array: two calls that overlap on the
- * GPU race.  Calls no allocating routine. */
+ * stream capture.  All calls share the array, which keeps the last call's
+ * contents; each call clears the array's split counters on its stream before
+ * the launch.  Two calls that overlap on the GPU race.  Calls no allocating
+ * routine. */
 int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* pool,
                                       int32_t layer, const int32_t* block_tables,
                                       const int32_t* table_rows, const int32_t* frontiers,

@@ -45,10 +45,6 @@ static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
   }
   const int per_sm = occ(D, pl->nqt, &pl->ring_bytes);
   pl->target = p->num_sms * per_sm / H;
-  // the merging CTA keeps R x D accumulators and R x splits weights in its
-  // stage ring
-  const int cap = (pl->ring_bytes / 4 - pl->R * D) / pl->R;
-  if (pl->target > cap) pl->target = cap;
   if (pl->target < 1) pl->target = 1;
   plan_sizes(pl, B, H, D);
   return NK_OK;
@@ -170,7 +166,10 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
-  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
+  // the scratch is shared by every call: its split counters start at zero
+  cudaError_t e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(B) * H * sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the split counters");
+  e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return NK_OK;
 }

@@ -106,14 +106,16 @@ struct DecodeCfg {
   static constexpr int Q_PITCH = D * 2 + 32;  // bytes per q row (padded against bank conflicts)
   // q fragments of a warp live in registers when they are few, else they are
   // read from shared memory (f16 / bf16 ready) at every k-step
-  static constexpr bool Q_SMEM = (D / NH / 16) * NQT * 2 > 32;
-  static constexpr int OFF_Q = NSTAGE * STAGE;
+  static constexpr bool Q_SMEM = (D / NH / 16) * NQT * 2 > 32 || NH == 2;
+  // the final combine keeps one [R][D] fp32 slice per key slab group (4)
+  static constexpr int COMB = 4 * R * D * 4;
+  static constexpr int OFF_Q = align_up(NSTAGE * STAGE > COMB ? NSTAGE * STAGE : COMB, 128);
   static constexpr int OFF_X = OFF_Q + align_up(R * Q_PITCH, 128);   // partial-S exchange [2][NW][32][NQT*4]
   static constexpr int OFF_RED = OFF_X + (NH == 2 ? 2 * NW * 32 * NQT * 4 * 4 : 0);
   static constexpr int OFF_BAR = OFF_RED + 10 * R * 4;  // m, l per pair; M, L per row
   static constexpr int MISC_INTS = 32;
   static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
-  static_assert(R * D * 4 <= NSTAGE * STAGE, "final combine reuses the stage ring");
+  static_assert(R * 32 * 12 <= OFF_Q, "merge weights of 32 splits fit below q");
   // CTAs per SM the register allocation aims at, from the O accumulators of
   // a warp ((D / NH) x R fp32 over 32 lanes).
   static constexpr int OREGS = (D / NH) * R / 32;
@@ -735,46 +737,57 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     row_L[tid] = Ls;
   }
   consumer_sync<NCONS>();
-  float* acc = reinterpret_cast<float*>(smem);  // [R][D], reuses the stage ring
-  float fac[NQT][2];
+  // every slab group writes its O, rescaled to the CTA max, into its own
+  // [R][D] slice (the stage ring is free now); the slices are then summed in
+  // a fixed order
+  float* comb = reinterpret_cast<float*>(smem);
+  {
+    float fac[NQT][2];
 #pragma unroll
-  for (int j = 0; j < NQT; ++j)
+    for (int j = 0; j < NQT; ++j)
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float M = row_M[8 * j + 2 * c + u];
-      fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
-    }
-  for (int w = 0; w < 4; ++w) {
-    if (pair == w) {
+      for (int u = 0; u < 2; ++u) {
+        const float M = row_M[8 * j + 2 * c + u];
+        fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
+      }
+    float* mine = comb + pair * R * D;
 #pragma unroll
-      for (int mt = 0; mt < MTW; ++mt)
+    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
-        for (int j = 0; j < NQT; ++j)
+      for (int j = 0; j < NQT; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qr = 8 * j + 2 * c + (e & 1), hi = e >> 1;
-            int d;
-            if constexpr (KV == KIND_BF16) d = half * DH + 16 * mt + r + 8 * hi;
-            else d = half * DH + 32 * (mt >> 1) + 4 * r + 2 * (mt & 1) + hi;
-            const float v = o[mt][j][e] * fac[j][e & 1];
-            if (w == 0) acc[qr * D + d] = v;
-            else acc[qr * D + d] += v;
-          }
-    }
-    consumer_sync<NCONS>();
+        for (int e = 0; e < 4; ++e) {
+          const int qr = 8 * j + 2 * c + (e & 1), hi = e >> 1;
+          int d;
+          if constexpr (KV == KIND_BF16) d = half * DH + 16 * mt + r + 8 * hi;
+          else d = half * DH + 32 * (mt >> 1) + 4 * r + 2 * (mt & 1) + hi;
+          mine[qr * D + d] = o[mt][j][e] * fac[j][e & 1];
+        }
   }
+  consumer_sync<NCONS>();
   const bool final_out = (nsplit == 1);
   const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
   const int64_t part = part0 + split;
-  for (int idx = tid; idx < R_real * D; idx += NCONS) {
-    const int qr = idx / D, d = idx % D;
+  for (int idx = tid; idx < R_real * (D / 4); idx += NCONS) {
+    const int qr = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    float4 v = *reinterpret_cast<const float4*>(comb + qr * D + d);
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(comb + (w * R + qr) * D + d);
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
     if (final_out) {
       const float L = row_L[qr];
+      const float inv = L > 0.f ? 1.f / L : 0.f;
       const int t = qr / a.G, g = qr % a.G;
-      a.out[((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d] =
-          __float2bfloat16_rn(L > 0.f ? acc[idx] / L : 0.f);
+      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(v.x * inv, v.y * inv), pack_bf16x2(v.z * inv, v.w * inv));
     } else {
-      a.ws_acc[(part * R + qr) * D + d] = acc[idx];
+      *reinterpret_cast<float4*>(a.ws_acc + (part * R + qr) * D + d) = v;
     }
   }
   if (tid < R_real) {
@@ -805,23 +818,26 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   consumer_sync<NCONS>();
   if (!s_flags[1]) return;
   __threadfence();
-  float* wgt = acc + R * D;  // [R_real][nsplit] merge weights, in the stage ring
+  // (m, l) of every split of every query row, one load each, to shared memory
+  // (the stage ring is free now); then one warp per row: nsplit <= 32 splits,
+  // one per lane
+  float2* sml = reinterpret_cast<float2*>(smem);                  // [R_real][nsplit]
+  float* wgt = reinterpret_cast<float*>(sml + R_real * nsplit);   // [R_real][nsplit]
+  for (int x = tid; x < R_real * nsplit; x += NCONS) {
+    const int qr = x / nsplit, k = x - qr * nsplit;
+    sml[x] = __ldcg(&a.ws_ml[(part0 + k) * R + qr]);
+  }
+  consumer_sync<NCONS>();
   for (int qr = warp; qr < R_real; qr += NW) {
-    float M = -INFINITY;
-    for (int k = lane; k < nsplit; k += 32) M = fmaxf(M, __ldcg(&a.ws_ml[(part0 + k) * R + qr]).x);
+    const float2 ml = lane < nsplit ? sml[qr * nsplit + lane] : make_float2(-INFINITY, 0.f);
+    float M = ml.x;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float Ls = 0.f;
-    if (M != -INFINITY)
-      for (int k = lane; k < nsplit; k += 32) {
-        const float2 ml = __ldcg(&a.ws_ml[(part0 + k) * R + qr]);
-        Ls += ml.y * ex2(ml.x - M);
-      }
+    const float e = M == -INFINITY ? 0.f : ex2(ml.x - M);
+    float Ls = ml.y * e;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int k = lane; k < nsplit; k += 32)
-      wgt[qr * nsplit + k] = Ls > 0.f ? ex2(__ldcg(&a.ws_ml[(part0 + k) * R + qr]).x - M) * inv : 0.f;
+    if (lane < nsplit) wgt[qr * nsplit + lane] = Ls > 0.f ? e / Ls : 0.f;
     if (lane == 0 && a.lse) {
       const int t = qr / a.G, g = qr % a.G;
       a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
@@ -829,28 +845,54 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     }
   }
   consumer_sync<NCONS>();
-  // four consecutive dims per thread (16-byte loads), splits unrolled by four
-  for (int idx = tid; idx < R_real * (D / 4); idx += NCONS) {
-    const int qr = idx / (D / 4), d = (idx % (D / 4)) * 4;
-    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (part0 * R + qr) * D + d);
-    const int64_t stride = static_cast<int64_t>(R) * D / 4;
-    const float* w = wgt + qr * nsplit;
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    int k = 0;
-    for (; k + 2 <= nsplit; k += 2) {
-      const float4 v0 = __ldcg(src + k * stride), v1 = __ldcg(src + (k + 1) * stride);
-      const float w0 = w[k], w1 = w[k + 1];
-      s0.x = fmaf(w0, v0.x, s0.x); s0.y = fmaf(w0, v0.y, s0.y); s0.z = fmaf(w0, v0.z, s0.z); s0.w = fmaf(w0, v0.w, s0.w);
-      s1.x = fmaf(w1, v1.x, s1.x); s1.y = fmaf(w1, v1.y, s1.y); s1.z = fmaf(w1, v1.z, s1.z); s1.w = fmaf(w1, v1.w, s1.w);
+  // out = sum_s w_s acc_s: four consecutive dims per item (16-byte loads); a
+  // thread takes IPT items and, per round, KB splits of each, so that about
+  // 16 independent loads are in flight per thread
+  {
+    constexpr int NIT = R * (D / 4);                  // items at most (R_real <= R)
+    constexpr int IPT = (NIT + NCONS - 1) / NCONS;
+    constexpr int KB = IPT >= 8 ? 2 : IPT >= 4 ? 4 : IPT >= 2 ? 8 : 16;
+    const int nit = R_real * (D / 4);
+    const int64_t stride = static_cast<int64_t>(R) * D / 4;  // float4 per split
+    const float4* base = reinterpret_cast<const float4*>(a.ws_acc + part0 * R * D);
+    float4 sum[IPT];
+#pragma unroll
+    for (int it = 0; it < IPT; ++it) sum[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < nsplit; k0 += KB) {
+      float4 v[IPT][KB];
+#pragma unroll
+      for (int it = 0; it < IPT; ++it) {
+        const int x = tid + it * NCONS;
+        const int qr = x / (D / 4), d4 = x % (D / 4);
+#pragma unroll
+        for (int u = 0; u < KB; ++u)
+          v[it][u] = (x < nit && k0 + u < nsplit) ? __ldcg(base + (k0 + u) * stride + qr * (D / 4) + d4)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int it = 0; it < IPT; ++it) {
+        const int x = tid + it * NCONS;
+        const int qr = x < nit ? x / (D / 4) : 0;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const float w = k0 + u < nsplit ? wgt[qr * nsplit + k0 + u] : 0.f;
+          sum[it].x = fmaf(w, v[it][u].x, sum[it].x);
+          sum[it].y = fmaf(w, v[it][u].y, sum[it].y);
+          sum[it].z = fmaf(w, v[it][u].z, sum[it].z);
+          sum[it].w = fmaf(w, v[it][u].w, sum[it].w);
+        }
+      }
     }
-    if (k < nsplit) {
-      const float4 v0 = __ldcg(src + k * stride);
-      const float w0 = w[k];
-      s0.x = fmaf(w0, v0.x, s0.x); s0.y = fmaf(w0, v0.y, s0.y); s0.z = fmaf(w0, v0.z, s0.z); s0.w = fmaf(w0, v0.w, s0.w);
+#pragma unroll
+    for (int it = 0; it < IPT; ++it) {
+      const int x = tid + it * NCONS;
+      if (x >= nit) continue;
+      const int qr = x / (D / 4), d = (x % (D / 4)) * 4;
+      const int t = qr / a.G, g = qr % a.G;
+      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(sum[it].x, sum[it].y), pack_bf16x2(sum[it].z, sum[it].w));
     }
-    const int t = qr / a.G, g = qr % a.G;
-    __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(s0.x + s1.x, s0.y + s1.y), pack_bf16x2(s0.z + s1.z, s0.w + s1.w));
   }
   if (tid == 0) a.counters[b * a.H + h] = 0;  // ready for the next call
 }
