@@ -809,9 +809,11 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   // out = sum_s acc_s 2^(m_s - M) / L, lse = (M + log2 L) ln 2: the softmax over
   // the union of the splits' keys.  Partials are published with a device-scope
   // fence before the counter increment; the last CTA reads them from L2.
-  __threadfence();
   consumer_sync<NCONS>();
   if (tid == 0) {
+    // one device-scope fence after the barrier makes every thread's partial
+    // stores visible before the counter increment
+    __threadfence();
     const int done = atomicAdd(&a.counters[b * a.H + h], 1);
     s_flags[1] = (done == nsplit - 1);
   }
