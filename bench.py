@@ -170,10 +170,11 @@ class Bench:
     """Device state of one workload; `share` reuses another Bench's filled
     pool (a sub-batch of its first B rows)."""
 
-    def __init__(self, w, device, B=None, share=None):
+    def __init__(self, w, device, B=None, share=None, fused=True):
         import torch
         from paged_kv_cache_append_gb300 import nk
         self.torch, self.nk, self.w, self.dev = torch, nk, w, device
+        self.fused = fused
         B = w.B if B is None else B
         self.B = B
         self.tables = torch.from_numpy(w.tables).to(device)
@@ -196,7 +197,8 @@ class Bench:
         self.lse = [torch.empty((B, w.T, w.Hq), dtype=torch.float32, device=device) for _ in self.q]
         n = nk.nk_decode_workspace_bytes(self.pool.handle, B, w.T, w.Hq)
         self.ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
-        self.launches_per_step = 2 * w.num_layers    # append + decode (merge in-kernel) per layer
+        # one fused append + decode launch per layer (merge in-kernel), or two
+        self.launches_per_step = (1 if fused else 2) * w.num_layers
         # chunked prefill rows (bf16_prefill): append the chunk, then attend
         self.Bp = len(w.prefill_rows) if share is None else 0
         if self.Bp:
@@ -254,10 +256,7 @@ class Bench:
                 for layer in range(w.num_layers):
                     self.prefill_only(layer, append=True)
         for layer in range(w.num_layers):
-            self.pool.append(layer, self.tables, self.rows, self.ctx, self.k[layer], self.v[layer],
-                             stream=stream)
-            self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
-                             out=self.out[layer], lse=self.lse[layer], workspace=self.ws, stream=stream)
+            self.attend(layer, stream)
 
         if self.Bp:
             torch.cuda.current_stream().wait_stream(self.side)
@@ -279,10 +278,32 @@ class Bench:
             tot += 4 * w.D * w.Hq * (P0 * S + S * (S + 1) // 2)
         return int(tot)
 
-    def decode_only(self, layer):
+    def attend(self, layer, stream=None):
+        """The decode step of one layer: append the new tokens, then attend
+        (one fused launch, or the two separate calls)."""
         w = self.w
-        self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
-                         out=self.out[layer], lse=self.lse[layer], workspace=self.ws)
+        if self.fused:
+            self.pool.append_decode(layer, self.q[layer], self.k[layer], self.v[layer], self.tables,
+                                    self.rows, self.front, w.scale, out=self.out[layer],
+                                    lse=self.lse[layer], workspace=self.ws, stream=stream)
+        else:
+            self.pool.append(layer, self.tables, self.rows, self.ctx, self.k[layer], self.v[layer],
+                             stream=stream)
+            self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
+                             out=self.out[layer], lse=self.lse[layer], workspace=self.ws, stream=stream)
+
+    def roofline_launch(self, layer):
+        """The dominant kernel of a decode layer: the fused append + decode
+        launch (or the plain decode launch when not fused)."""
+        w = self.w
+        if self.fused:
+            self.attend(layer)
+        else:
+            self.pool.decode(layer, self.q[layer], self.tables, self.rows, self.front, w.scale,
+                             out=self.out[layer], lse=self.lse[layer], workspace=self.ws)
+
+    def bytes_roofline_launch(self):
+        return self.bytes_decode_layer() + (self.bytes_append_layer() if self.fused else 0)
 
     # -- accounting --------------------------------------------------------
     def bytes_decode_layer(self):
@@ -320,7 +341,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(device)
     w = make_workload(args.workload, args.layers, args.context)
     hbm_peak, peak_kind = peaks()
-    bench = Bench(w, device)
+    bench = Bench(w, device, fused=not args.unfused)
     flush, flush_bytes = _flush_fn(torch, device)
     stream = torch.cuda.current_stream()
 
@@ -360,19 +381,19 @@ def run_gpu(args, rank, world):
         ms = float(t.item())
     clocks = clk.summary()
 
-    # ---- dominant kernel: one decode launch (decode + merge), per layer ----
+    # ---- dominant kernel: one (append +) decode launch, per layer ------------
     kev = []
     for _ in range(max(3, args.steps // 2)):
         for layer in range(w.num_layers):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             flush()
             e0.record(stream)
-            bench.decode_only(layer)
+            bench.roofline_launch(layer)
             e1.record(stream)
             kev.append((e0, e1))
     torch.cuda.synchronize()
     kms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in kev)
-    achieved = bench.bytes_decode_layer() / (kms * 1e-3) / 1e9
+    achieved = bench.bytes_roofline_launch() / (kms * 1e-3) / 1e9
 
     # ---- prefill kernel (bf16_prefill): tensor roofline ---------------------------
     prefill_line = None
@@ -449,7 +470,7 @@ def run_gpu(args, rank, world):
     sweep = {}
     if not args.no_sweep and w.B > 1:
         for c in range(1, w.B + 1):
-            bc = Bench(w, device, B=c, share=bench) if c != w.B else bench
+            bc = Bench(w, device, B=c, share=bench, fused=bench.fused) if c != w.B else bench
             g = torch.cuda.CUDAGraph()
             bc.step()
             torch.cuda.synchronize()
@@ -472,6 +493,7 @@ def run_gpu(args, rank, world):
                              "ms_per_step": round(sm, 4)}
             del bc
 
+    roof_kernel = "nk_paged_append_decode_attention" if bench.fused else "nk_paged_decode_attention"
     value = world * bench.bytes_step() / (ms * 1e-3) / 1e9
     e2e_val = world * bench.bytes_step() / (e2e_ms * 1e-3) / 1e9
     line = {
@@ -491,17 +513,20 @@ def run_gpu(args, rank, world):
         "config": {"workload": workload_desc(w), "rows": bench.B, "layers": w.num_layers,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"flushed ({flush_bytes >> 20} MiB write) before every timed step",
-                   "graph": "one CUDA graph per step"},
+                   "graph": "one CUDA graph per step",
+                   "step": ("fused append + decode launch per layer" if bench.fused
+                            else "append launch + decode launch per layer")},
         "rows_per_s": round(bench.B * w.T / (ms * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": (traffic(args.workload, "nk_paged_decode_attention", bench.bytes_decode_layer())
+                     "traffic": (traffic(args.workload, roof_kernel, bench.bytes_roofline_launch())
                                  if not bench.Bp else None),
                      "traffic_unit": "bytes per launch",
-                     "kernel": "nk_paged_decode_attention (decode + merge), one layer",
-                     "algorithmic_bytes_per_launch": bench.bytes_decode_layer(),
+                     "kernel": roof_kernel + (" (append + decode + merge)" if bench.fused
+                                              else " (decode + merge)") + ", one layer",
+                     "algorithmic_bytes_per_launch": bench.bytes_roofline_launch(),
                      "avg_launch_ms": round(kms, 5)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
@@ -609,6 +634,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling)")
     ap.add_argument("--context", type=int, default=None, help="smaller max context S (profiling)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate append and decode launches instead of the fused call")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

@@ -193,6 +193,26 @@ int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, in
                               float softmax_scale, void* out, float* lse, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* nk_paged_kv_append followed by nk_paged_decode_attention in one launch: the
+ * T new tokens of every row are written at positions F_b - T .. F_b - 1
+ * (write_pos = frontiers - T), with the codec rules of nk_paged_kv_append,
+ * and then attended together with the rest of the row.  The decode step of
+ * the engine page's compact batch is exactly this pair ("Paged KV cache"
+ * page: codes and scales are complete before the frontier is published;
+ * "Engine architecture" page: compact decode batch).  Each CTA encodes the
+ * new tokens whose pages it reads and orders those stores before its own TMA
+ * reads of the pages, so no other kernel or host step is involved.
+ *   k, v: device bf16 [B][T][H][D] (16-byte aligned); other arguments and
+ *   the workspace contract as in nk_paged_decode_attention.
+ * A row with F_b < T is rejected on the device (status NK_STATUS_FRONTIER,
+ * nothing written, out = 0, lse = -inf).  Errors: as nk_paged_decode_attention. */
+int nk_paged_append_decode_attention(const void* q, int32_t Hq, nk_pool* pool, int32_t layer,
+                                     const int32_t* block_tables, const int32_t* table_rows,
+                                     const int32_t* frontiers, const void* k, const void* v,
+                                     int32_t B, int32_t T, float softmax_scale, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* Size of the static device scratch of nk_paged_decode_attention_noalloc. */
 #define NK_NOALLOC_SCRATCH_BYTES (32u << 20)
 

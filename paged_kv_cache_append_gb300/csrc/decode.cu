@@ -65,18 +65,23 @@ extern "C" int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t
   return NK_OK;
 }
 
-extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool,
-                                         int32_t layer, const int32_t* block_tables,
-                                         const int32_t* table_rows, const int32_t* frontiers,
-                                         int32_t B, int32_t T, float softmax_scale, void* out,
-                                         float* lse, void* workspace, size_t workspace_bytes,
-                                         void* stream) {
-  clear_error();
+namespace nk {
+
+// Shared by the decode entry points: checks, plan, arguments, launch.
+// k_new / v_new non-null: fused append of the T new tokens first.
+static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,
+                      const int32_t* block_tables, const int32_t* table_rows,
+                      const int32_t* frontiers, const void* k_new, const void* v_new, int32_t B,
+                      int32_t T, float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, cudaStream_t s, const char* what) {
   if (!q || !pool || !block_tables || !table_rows || !frontiers || !out)
-    return fail(NK_ERR_INVALID_ARG, "null argument to nk_paged_decode_attention");
+    return fail(NK_ERR_INVALID_ARG, std::string("null argument to ") + what);
   if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
   if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
   if (!aligned16(q) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
+  if ((k_new != nullptr) != (v_new != nullptr)) return fail(NK_ERR_INVALID_ARG, "k and v come together");
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(NK_ERR_ALIGN, "k / v must be 16-byte aligned");
   DecodePlan pl;
   int rc = make_plan(pool, B, T, Hq, &pl);
   if (rc) return rc;
@@ -107,10 +112,46 @@ extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_poo
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (k_new) {
+    a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    a.kc_w = static_cast<uint8_t*>(pool->ptrs[layer * np + 0]);
+    a.vc_w = static_cast<uint8_t*>(pool->ptrs[layer * np + 1]);
+    a.ks_w = np == 4 ? static_cast<uint8_t*>(pool->ptrs[layer * np + 2]) : nullptr;
+    a.vs_w = np == 4 ? static_cast<uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
+  }
   cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return NK_OK;
+}
+
+}  // namespace nk
+
+extern "C" int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool,
+                                         int32_t layer, const int32_t* block_tables,
+                                         const int32_t* table_rows, const int32_t* frontiers,
+                                         int32_t B, int32_t T, float softmax_scale, void* out,
+                                         float* lse, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  clear_error();
+  return run_decode(q, Hq, pool, layer, block_tables, table_rows, frontiers, nullptr, nullptr, B, T,
+                    softmax_scale, out, lse, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream), "nk_paged_decode_attention");
+}
+
+extern "C" int nk_paged_append_decode_attention(const void* q, int32_t Hq, nk_pool* pool,
+                                                int32_t layer, const int32_t* block_tables,
+                                                const int32_t* table_rows,
+                                                const int32_t* frontiers, const void* k,
+                                                const void* v, int32_t B, int32_t T,
+                                                float softmax_scale, void* out, float* lse,
+                                                void* workspace, size_t workspace_bytes,
+                                                void* stream) {
+  clear_error();
+  if (!k || !v) return fail(NK_ERR_INVALID_ARG, "null k / v to nk_paged_append_decode_attention");
+  return run_decode(q, Hq, pool, layer, block_tables, table_rows, frontiers, k, v, B, T, softmax_scale,
+                    out, lse, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                    "nk_paged_append_decode_attention");
 }
 
 namespace nk {

@@ -39,6 +39,7 @@
 #pragma once
 
 #include "device.cuh"
+#include "encode.cuh"
 #include "internal.h"
 
 namespace nk {
@@ -59,6 +60,15 @@ struct DecodeArgs {
   float* ws_acc;  // [B][H][maxsplit][R][D]
   int* counters;  // [B][H] splits finished; zero between calls (the last CTA resets it)
   int* status;
+  // Fused append (nullptr: plain decode): the T new tokens of row b, bf16
+  // [B][T][H][D], are encoded into positions F_b - T .. F_b - 1 of the
+  // writable planes before the pages holding them are read.
+  const __nv_bfloat16* k_new = nullptr;
+  const __nv_bfloat16* v_new = nullptr;
+  uint8_t* kc_w = nullptr;
+  uint8_t* vc_w = nullptr;
+  uint8_t* ks_w = nullptr;
+  uint8_t* vs_w = nullptr;
   float softmax_scale;
   int B, T, Hq, H, G, L, M, C;
   int target;    // splits per head the chunking aims at (= maxsplit)
@@ -114,7 +124,7 @@ struct DecodeCfg {
   static constexpr int OFF_RED = OFF_X + (NH == 2 ? 2 * NW * 32 * NQT * 4 * 4 : 0);
   static constexpr int OFF_BAR = OFF_RED + 10 * R * 4;  // m, l per pair; M, L per row
   static constexpr int MISC_INTS = 32;
-  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
+  static constexpr int SMEM = OFF_BAR + (2 * NSTAGE + 1) * 8 + MISC_INTS * 4 + 1024;  // + alignment slack
   static_assert(R * 32 * 12 <= OFF_Q, "merge weights of 32 splits fit below q");
   // CTAs per SM the register allocation aims at, from the O accumulators of
   // a warp ((D / NH) x R fp32 over 32 lanes).
@@ -186,7 +196,8 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   float* row_L = row_M + R;                                         // [R]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
-  int* s_flags = reinterpret_cast<int*>(empty + NSTAGE);    // [0] abort, [1] merging CTA
+  uint64_t* app = empty + NSTAGE;                           // fused append done (NW arrivals)
+  int* s_flags = reinterpret_cast<int*>(app + 1);           // [0] abort, [1] merging CTA
   int* s_F = s_flags + 4;                                   // [8] valid length per row
   int* s_row = s_flags + 12;                                // [8] table row per row
   float* s_qmax = reinterpret_cast<float*>(s_flags + 20);   // [8] per-warp max|q|
@@ -202,6 +213,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NW);
     }
+    mbar_init(app, NW);
     s_flags[0] = 0;
     s_flags[1] = 0;
     fence_barrier_init();
@@ -216,7 +228,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   // ---- per-row lengths, loaded once in parallel ------------------------------
   if (tid < a.B) {
     const int F = a.frontiers[tid], row = a.table_rows[tid];
-    const bool ok = F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C;
+    const bool ok = F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C && (a.k_new == nullptr || F >= a.T);
     if (!ok && blockIdx.x == 0 && h == 0) set_status(a.status, NK_STATUS_FRONTIER);
     s_F[tid] = ok ? F : 0;
     s_row[tid] = ok ? row : 0;
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     int acc = 0;
     for (int bb = 0; bb < a.B; ++bb) {
       const int np = (s_F[bb] + 63) >> 6;
-      const int ns = (np + chunk - 1) / chunk;
+      const int ns = max(1, (np + chunk - 1) / chunk);  // a row without keys still writes out / lse
       if (static_cast<int>(blockIdx.x) < acc + ns) {
         b = bb;
         split = blockIdx.x - acc;
@@ -250,20 +262,27 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   if (b < 0) return;
   const int F = s_F[b];
   const int p0 = split * chunk;
-  const int n = min(chunk, npages - p0);  // pages of this CTA (>= 1)
+  const int n = min(chunk, npages - p0);  // pages of this CTA (0 only for a row without keys)
+  const bool fused = a.k_new != nullptr;
+  const int app_lo = fused ? (F - a.T) >> 6 : 0x7fffffff;  // first page that receives new tokens
   const int R_real = a.T * a.G;
 
   // ---- producer warp: stage pages p0 .. p0+n-1 ---------------------------------
   if (warp == NW) {
     const int32_t* table = a.tables + static_cast<int64_t>(s_row[b]) * a.L + p0;
     int gnext = 0;
+    bool app_seen = false;
     for (int i = 0; i < n; ++i) {
       if ((i & 31) == 0) gnext = (i + lane < n) ? table[i + lane] : 0;  // 32 table entries per load
       int g = __shfl_sync(0xffffffffu, gnext, i & 31);
       int stop = 0;
       if (lane == 0) {
         const int s = i % NSTAGE;
-        if (i >= NSTAGE && !mbar_wait_bounded(&empty[s], ((i / NSTAGE) - 1) & 1, a.status)) {
+        if (p0 + i >= app_lo && !app_seen) {  // this page receives new tokens: wait for them
+          app_seen = true;
+          if (!mbar_wait_bounded(app, 0, a.status)) stop = 1;
+        }
+        if (stop || (i >= NSTAGE && !mbar_wait_bounded(&empty[s], ((i / NSTAGE) - 1) & 1, a.status))) {
           s_flags[0] = 1;
           stop = 1;
         } else {
@@ -289,6 +308,33 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       if (__shfl_sync(0xffffffffu, stop, 0)) break;
     }
     return;  // the copies complete into the shared memory of the still-running CTA
+  }
+
+  // ---- fused append: the new tokens whose pages this CTA reads ------------------
+  // One consumer warp per token encodes its K and V rows of head h into the
+  // pool, then orders those generic-proxy stores before the producer's TMA
+  // reads of the same bytes (fence.proxy.async + the app mbarrier).
+  if (fused) {
+    constexpr int KCBW = code_row_bytes<KK>(D), VCBW = code_row_bytes<KV>(D);
+    constexpr int KSBW = scale_row_bytes<KK>(D), VSBW = scale_row_bytes<KV>(D);
+    const int32_t* trow = a.tables + static_cast<int64_t>(s_row[b]) * a.L;
+    for (int t = warp; t < a.T; t += NW) {
+      const int pos = F - a.T + t;
+      const int pg = pos >> 6;
+      if (pg < p0 || pg >= p0 + n) continue;
+      const int g = trow[pg];
+      if (g < 0 || g >= a.M) {
+        if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
+        continue;
+      }
+      const int64_t token_row = (static_cast<int64_t>(g) * a.H + h) * 64 + (pos & 63);
+      const int64_t src = ((static_cast<int64_t>(b) * a.T + t) * a.H + h) * D;
+      encode_row<KK, D>(a.k_new + src, a.kc_w + token_row * KCBW, a.ks_w ? a.ks_w + token_row * KSBW : nullptr, lane);
+      encode_row<KV, D>(a.v_new + src, a.vc_w + token_row * VCBW, a.vs_w ? a.vs_w + token_row * VSBW : nullptr, lane);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(app);
   }
 
   // ---- q rows to shared memory (16-byte loads) and the f16 prescale --------------

@@ -27,7 +27,8 @@ POOL_CHECK_BOUNDS = 1
 
 SYMBOLS = ["nk_version", "nk_last_error", "nk_pool_plane_bytes", "nk_pool_capacity_bounds",
            "nk_pool_create", "nk_pool_destroy", "nk_paged_kv_append", "nk_decode_workspace_bytes",
-           "nk_paged_decode_attention", "nk_paged_decode_attention_noalloc",
+           "nk_paged_decode_attention", "nk_paged_append_decode_attention",
+           "nk_paged_decode_attention_noalloc",
            "nk_prefill_workspace_bytes", "nk_paged_prefill_attention",
            "nk_page_copy_columns", "nk_status_read"]
 
@@ -67,6 +68,8 @@ def load(path: str | None = None) -> C.CDLL:
         "nk_paged_kv_append": (C.c_int, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
         "nk_decode_workspace_bytes": (C.c_int, [_P, _I, _I, _I, C.POINTER(_S)]),
         "nk_paged_decode_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
+        "nk_paged_append_decode_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _F, _P, _P, _P,
+                                                       _S, _P]),
         "nk_paged_decode_attention_noalloc": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P]),
         "nk_prefill_workspace_bytes": (C.c_int, [_P, _I, _I, _I, C.POINTER(_S)]),
         "nk_paged_prefill_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
@@ -137,6 +140,13 @@ def nk_paged_decode_attention(q, Hq, pool, layer, block_tables, table_rows, fron
                               out, lse, workspace, workspace_bytes, stream):
     _check(load().nk_paged_decode_attention(q, Hq, pool, layer, block_tables, table_rows, frontiers,
                                             B, T, scale, out, lse, workspace, workspace_bytes, stream))
+
+
+def nk_paged_append_decode_attention(q, Hq, pool, layer, block_tables, table_rows, frontiers, k, v, B,
+                                     T, scale, out, lse, workspace, workspace_bytes, stream):
+    _check(load().nk_paged_append_decode_attention(q, Hq, pool, layer, block_tables, table_rows,
+                                                   frontiers, k, v, B, T, scale, out, lse, workspace,
+                                                   workspace_bytes, stream))
 
 
 def nk_paged_decode_attention_noalloc(q, Hq, pool, layer, block_tables, table_rows, frontiers, B, T,
@@ -241,6 +251,22 @@ class Pool:
         nk_paged_decode_attention(_ptr(q), Hq, self.handle, layer, _ptr(tables), _ptr(table_rows),
                                   _ptr(frontiers), B, T, float(scale), _ptr(out), _ptr(lse),
                                   _ptr(ws), ws.numel(), _stream(stream))
+        return out, lse
+
+    def append_decode(self, layer, q, k, v, tables, table_rows, frontiers, scale, out=None, lse=None,
+                      workspace=None, stream=None):
+        """Appends the T new tokens k, v [B, T, H, D] of every row at
+        frontiers - T .. frontiers - 1, then attends (one launch)."""
+        import torch
+        B, T, Hq, D = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+        ws = workspace if workspace is not None else self.workspace(B, T, Hq)
+        nk_paged_append_decode_attention(_ptr(q), Hq, self.handle, layer, _ptr(tables), _ptr(table_rows),
+                                         _ptr(frontiers), _ptr(k), _ptr(v), B, T, float(scale), _ptr(out),
+                                         _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
         return out, lse
 
     def prefill(self, layer, q, tables, table_rows, prefix_len, chunk_len, scale, out=None,

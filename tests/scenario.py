@@ -95,8 +95,9 @@ class Scenario:
                             bf16_to_bits(k), bf16_to_bits(v), counts=counts)
 
     # -- decode step ---------------------------------------------------------
-    def step(self, layer, out=None, lse=None):
-        """Appends the step tokens of the decode rows and runs the GPU decode.
+    def step(self, layer, out=None, lse=None, fused=False):
+        """Appends the step tokens of the decode rows and runs the GPU decode
+        (fused=True: both in one nk_paged_append_decode_attention call).
         Returns (q, out, lse, frontiers) with q on the CPU."""
         w = self.w
         k, v = w.step_kv(layer)
@@ -105,10 +106,14 @@ class Scenario:
         tr = torch.from_numpy(w.table_rows).to(dev)
         wp = torch.from_numpy(w.context).to(dev)
         fr = torch.from_numpy(w.context + w.T).to(dev)
-        self.gpu.append(layer, self.tables_d, tr, wp, k.to(dev), v.to(dev))
         if self.orc is not None:
             self.orc.append(layer, w.tables, w.table_rows, w.context, bf16_to_bits(k), bf16_to_bits(v))
-        o, l = self.gpu.decode(layer, q.to(dev), self.tables_d, tr, fr, w.scale, out=out, lse=lse)
+        if fused:
+            o, l = self.gpu.append_decode(layer, q.to(dev), k.to(dev), v.to(dev), self.tables_d, tr, fr,
+                                          w.scale, out=out, lse=lse)
+        else:
+            self.gpu.append(layer, self.tables_d, tr, wp, k.to(dev), v.to(dev))
+            o, l = self.gpu.decode(layer, q.to(dev), self.tables_d, tr, fr, w.scale, out=out, lse=lse)
         torch.cuda.synchronize()
         return q, o.cpu(), l.cpu(), w.context + w.T
 

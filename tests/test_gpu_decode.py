@@ -27,9 +27,9 @@ def small(profile, Hkv, G, D, S, C, T, seed, contexts=None, layers=1, outliers=T
                       outlier_p=0.01 if outliers else 0.0, outlier_mul=20.0)
 
 
-def run_and_check(w, layer=0, strict=False):
+def run_and_check(w, layer=0, strict=False, fused=False):
     sc = Scenario(w, layers=(layer,))
-    q, out, lse, fr = sc.step(layer)
+    q, out, lse, fr = sc.step(layer, fused=fused)
     bad = sc.planes_equal(layer)
     assert not bad, f"plane mismatch (plane, count, first index, gpu, oracle): {bad}"
     ref_out, ref_lse = sc.oracle_decode(layer, q, fr)
@@ -58,6 +58,54 @@ def test_small_shapes(profile, D, G, T):
     w = small(profile, 2, G, D, 300, 3, T, seed=D * 10 + G + T,
               contexts=[0, 137, 300 - T])
     run_and_check(w)
+
+
+@pytest.mark.parametrize("profile", ["bf16", "int8_g64", "fp8_row", "nvfp4_g16", "k8v4"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G,T", [(8, 1), (2, 4), (8, 2)])
+def test_fused_append_decode(profile, D, G, T):
+    """nk_paged_append_decode_attention: the new tokens' codes are bit-exact
+    (the whole layer's planes equal the oracle's) and the attention that reads
+    them in the same launch matches the oracle."""
+    if D == 256 and G * T > 16:
+        pytest.skip("head_dim 256 supports T*G <= 16")
+    w = small(profile, 2, G, D, 300, 3, T, seed=D * 10 + G + T + 1, contexts=[0, 137, 300 - T])
+    run_and_check(w, fused=True)
+
+
+@pytest.mark.parametrize("profile", ["int8_g64", "k8v4"])
+def test_fused_new_tokens_straddle_pages_and_splits(profile):
+    """T = 4 new tokens that straddle a page boundary (positions 126..129 and
+    62..65), so that two CTAs of one row each encode part of them; plus rows
+    long enough to be split."""
+    w = small(profile, 4, 8, 128, 4096, 8, 4, seed=43,
+              contexts=[126, 62, 0, 1020, 2046, 3000, 4092, 190])
+    run_and_check(w, fused=True)
+
+
+def test_fused_int8_decode_workload_one_layer():
+    """The INT8-G64 decode workload's layer through the fused call."""
+    run_and_check(W.int8_decode(num_layers=1), fused=True)
+
+
+def test_row_without_keys_gets_zero_output():
+    """A row whose frontier is 0 has no key: out = 0 and lse = -inf (the
+    oracle's empty-set reading); the other rows are unaffected."""
+    w = small("int8_g64", 2, 8, 128, 1024, 3, 1, seed=71, contexts=[0, 100, 700])
+    sc = Scenario(w)
+    dev = "cuda"
+    q = w.step_q(0)
+    tr = torch.from_numpy(w.table_rows).to(dev)
+    fr_np = w.context.astype(np.int32)      # the filled context only; row 0 holds none
+    fr = torch.from_numpy(fr_np).to(dev)
+    out = torch.full((w.B, 1, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((w.B, 1, w.Hq), float("nan"), dtype=torch.float32, device=dev)
+    sc.gpu.decode(0, q.to(dev), sc.tables_d, tr, fr, w.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    out, lse = out.cpu(), lse.cpu()
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    ref_out, ref_lse = sc.oracle_decode(0, q, fr_np)
+    compare_attention(out, lse, ref_out, ref_lse)
 
 
 @pytest.mark.parametrize("profile", ["int8_g64", "k8v4"])
