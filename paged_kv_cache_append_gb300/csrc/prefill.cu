@@ -1,5 +1,5 @@
 // prefill.cu -- chunked prefill / replay attention through the block tables on
-// the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+// the 5th-generation tensor cores (tcgen05, operands and accumulators in TMEM).
 //
 // Contract: query i < chunk_len[b] of row b sits at logical position
 // prefix_len[b] + i and attends keys j <= prefix_len[b] + i of its table row
@@ -12,23 +12,28 @@
 // consecutive chunk tokens times the G query heads that share KV head h, so
 // every K / V page tile is loaded once for all of them.  Keys advance one page
 // (64 keys) at a time, which is also the P = 64 pipeline unit:
-//   S   = Q K^T   tcgen05.mma, M 128 x N 64 x K D, A = Q (shared, K-major,
-//                 128-byte swizzle), B = K page tile (shared, K-major), fp32
-//                 accumulator in TMEM (two buffers, ping-pong);
-//   P   = exp2(S * scale * log2 e - m) in bf16, written to TMEM by the four
-//                 softmax warps (one TMEM lane = one query row each);
+//   S   = Q K^T   tcgen05.mma, M 128 x N 64 x K D, A = Q (TMEM, written once
+//                 by the softmax warps), B = K page tile (shared, K-major,
+//                 128-byte swizzle), fp32 accumulator in TMEM (two buffers);
+//   P   = exp2(S * scale * log2 e - m) in bf16, written by the four softmax
+//                 warps (one TMEM lane = one query row each) over the first
+//                 32 columns of the S buffer it was computed from;
 //   O  += P V     tcgen05.mma, M 128 x N D x K 64, A = P (TMEM), B = V page
 //                 tile (shared, MN-major), fp32 accumulator in TMEM.
-// The running max is rescaled lazily: O is rescaled only when the row max
-// grows by more than 2^8, so P stays below 256 and fp32 O never overflows.
+// With both A operands in TMEM, the only shared-memory operand traffic is the
+// K and V page tiles.  The MMAs of one thread execute in issue order, so the
+// next S into a buffer (issued after the PV that reads its P) cannot overwrite
+// P early.  The running max is rescaled lazily: O is rescaled only when the
+// row max grows by more than 2^8, so P stays below 256 and fp32 O never
+// overflows.
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue, warp 4 TMA
-// producer (Q once, then K and V page tiles through two rings), warp 5 the
+// TMEM columns: S buffers [0, 64) and [64, 128), Q [128, 128 + D/2),
+// O [256, 256 + D).
+//
+// Warp roles (192 threads): warps 0-3 softmax and epilogue (and the Q copy to
+// TMEM), warp 4 TMA producer (K and V page tiles through two rings), warp 5 the
 // single MMA-issuing thread.  All waits are bounded.
-#include <cudaTypedefs.h>
-
 #include <cmath>
-#include <mutex>
 
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -36,6 +41,7 @@
 namespace nk {
 
 struct PrefillArgs {
+  const __nv_bfloat16* q;  // [B][Tc][Hq][D]
   const int32_t* tables;
   const int32_t* table_rows;
   const int32_t* prefix_len;
@@ -50,29 +56,20 @@ struct PrefillArgs {
 template <int D>
 struct PrefillCfg {
   static constexpr int THREADS = 192;
-  static constexpr int NK = D == 256 ? 2 : 3;  // K ring
-  static constexpr int NV = D == 256 ? 2 : 3;  // V ring
-  static constexpr int Q_BYTES = 128 * D * 2;  // 128 rows, D/64 column blocks of 16 KB
+  static constexpr int NK = D == 256 ? 3 : 6;  // K ring
+  static constexpr int NV = D == 256 ? 3 : 6;  // V ring
   static constexpr int KV_BYTES = 64 * D * 2;  // one page tile, D/64 column blocks of 8 KB
-  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
+  static constexpr int NBAR = 2 * NK + 2 * NV + 2 + 4;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 64 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 256;
+  static constexpr uint32_t COL_S = 0, COL_Q = 128, COL_O = 256;
   static constexpr uint32_t ID_S = tc::idesc_bf16(128, 64, false, false);
   static constexpr uint32_t ID_O = tc::idesc_bf16(128, D, false, true);
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
-
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ void arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -80,26 +77,24 @@ __device__ __forceinline__ void arrive(uint64_t* bar) {
 
 template <int D>
 __global__ void __launch_bounds__(192, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, PrefillArgs a) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   PrefillArgs a) {
   using Cfg = PrefillCfg<D>;
   constexpr int NK = Cfg::NK, NV = Cfg::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
   uint8_t* sK = smem + Cfg::OFF_K;
   uint8_t* sV = smem + Cfg::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
+  uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
   uint64_t* s_full = v_empty + NV;   // [2]
-  uint64_t* s_empty = s_full + 2;    // [2]
-  uint64_t* p_full = s_empty + 2;    // [1]  (+1 spare)
-  uint64_t* o_done = p_full + 2;     // [1]  (+1 spare)
-  uint64_t* drain = o_done + 2;      // [1]
+  uint64_t* p_full = s_full + 2;     // [1]
+  uint64_t* o_done = p_full + 1;     // [1]
+  uint64_t* q_ready = o_done + 1;    // [1]
+  uint64_t* drain = q_ready + 1;     // [1]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -124,7 +119,6 @@ __global__ void __launch_bounds__(192, 1)
   const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < NK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -133,16 +127,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
+    mbar_init(q_ready, 4);
     mbar_init(drain, 1);
     *s_abort = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
   }
@@ -158,12 +150,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     int gnext = 0;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, Cfg::Q_BYTES);
-#pragma unroll
-      for (int kb = 0; kb < D / 64; ++kb)
-        tma_load_3d(sQ + kb * 16384, &tmq, kb * 64, h * G, b * a.Tc + t0, q_full);
-    }
     for (int j = 0; j < nkt; ++j) {
       if ((j & 31) == 0) gnext = (j + lane < nkt) ? table[j + lane] : 0;
       int g = __shfl_sync(0xffffffffu, gnext, j & 31);
@@ -196,38 +182,33 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 5) {
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(q_full, 0, a.status);
+      bool ok = mbar_wait_bounded(q_ready, 0, a.status);
       tc::fence_after();
-      const uint32_t qbase = smem_u32(sQ);
       for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {
+        if (j < nkt) {  // S(j) = Q K(j)^T into buffer j & 1
           const int ks = j % NK, sb = j & 1;
           ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status);
-          if (ok && j >= 2) ok = mbar_wait_bounded(&s_empty[sb], ((j / 2) - 1) & 1, a.status);
           if (!ok) break;
           tc::fence_after();
-          const uint32_t kbase = smem_u32(sK + ks * Cfg::KV_BYTES);
+          const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::KV_BYTES), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc(qbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-            tc::mma_ss(tmem + Cfg::COL_S + 64 * sb, ad, bd, Cfg::ID_S, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)  // 16 dims: 8 TMEM columns of Q, 32 bytes of a K row
+            tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
+                       kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
           tc::commit(&s_full[sb]);
           tc::commit(&k_empty[ks]);
         }
-        if (j >= 1) {  // O += P V for page j - 1
+        if (j >= 1) {  // O += P(j - 1) V(j - 1), P in the first 32 columns of buffer (j - 1) & 1
           const int jj = j - 1, vs = jj % NV;
           ok = mbar_wait_bounded(&v_full[vs], (jj / NV) & 1, a.status);
           if (ok) ok = mbar_wait_bounded(p_full, jj & 1, a.status);
           if (!ok) break;
           tc::fence_after();
-          const uint32_t vbase = smem_u32(sV + vs * Cfg::KV_BYTES);
+          const uint64_t vd = tc::smem_desc(smem_u32(sV + vs * Cfg::KV_BYTES), 8192, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = tc::smem_desc(vbase + kk * 2048, 8192, 1024);
-            tc::mma_ts(tmem + Cfg::COL_O, tmem + Cfg::COL_P + kk * 8, bd, Cfg::ID_O, (jj > 0 || kk > 0));
-          }
+          for (int kk = 0; kk < 4; ++kk)  // 16 keys: 8 TMEM columns of P, 2 KB of V rows
+            tc::mma_ts(tmem + Cfg::COL_O, tmem + Cfg::COL_S + 64 * (jj & 1) + kk * 8,
+                       vd + static_cast<uint64_t>((kk * 2048) >> 4), Cfg::ID_O, (jj > 0 || kk > 0));
           tc::commit(o_done);
           tc::commit(&v_empty[vs]);
         }
@@ -243,7 +224,31 @@ __global__ void __launch_bounds__(192, 1)
     const bool row_valid = token < chunk;
     const int pos = prefix + token;  // keys <= pos are visible
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Q row m to TMEM columns [COL_Q, COL_Q + D/2): column c holds dims 2c, 2c+1
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g) * D);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = row_valid ? src[c0 / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * u] = x.x;
+          qv[4 * u + 1] = x.y;
+          qv[4 * u + 2] = x.z;
+          qv[4 * u + 3] = x.w;
+        }
+        tc::st32(tmem + lane_base + Cfg::COL_Q + c0, qv);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(q_ready);
+    }
     float m_used = -INFINITY, l = 0.f;
+    const bool pos_scale = a.scale_log2 >= 0.f;
+    const float fill = pos_scale ? -INFINITY : INFINITY;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
       const int sb = j & 1;
@@ -254,19 +259,28 @@ __global__ void __launch_bounds__(192, 1)
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb, v0);
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb + 32, v1);
       tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) arrive(&s_empty[sb]);
-      // scores in base 2 with the causal mask at absolute positions
+      // The row maximum of the scaled scores is the scale times the largest
+      // raw score (the smallest one for a negative scale); masked keys get the
+      // fill value that no extremum picks and whose exponent is 0.  The causal
+      // mask is applied only where the page reaches past a row's last key.
       const int kmax = row_valid ? pos - 64 * j : -1;  // keys c <= kmax of this page are visible
-      float s[64];
-      float rmax = -INFINITY;
+      float rext = fill;
+      if (__all_sync(0xffffffffu, kmax >= 63)) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = c <= kmax ? __uint_as_float(v0[c]) * a.scale_log2 : -INFINITY;
-        s[32 + c] = 32 + c <= kmax ? __uint_as_float(v1[c]) * a.scale_log2 : -INFINITY;
-        rmax = fmaxf(rmax, fmaxf(s[c], s[32 + c]));
+        for (int c = 0; c < 32; ++c) {
+          const float x = __uint_as_float(v0[c]), y = __uint_as_float(v1[c]);
+          rext = pos_scale ? fmaxf(rext, fmaxf(x, y)) : fminf(rext, fminf(x, y));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c > kmax) v0[c] = __float_as_uint(fill);
+          if (32 + c > kmax) v1[c] = __float_as_uint(fill);
+          const float x = __uint_as_float(v0[c]), y = __uint_as_float(v1[c]);
+          rext = pos_scale ? fmaxf(rext, fmaxf(x, y)) : fminf(rext, fminf(x, y));
+        }
       }
+      const float rmax = rext == fill ? -INFINITY : rext * a.scale_log2;
       float factor = 1.f;
       const float mnew = fmaxf(m_used, rmax);
       bool resc = false;
@@ -279,18 +293,24 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t pk[32];
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float pa = ex2(s[2 * c] - mu), pb = ex2(s[2 * c + 1] - mu);
-        sum += pa + pb;
+      for (int c = 0; c < 16; ++c) {
+        const float pa = ex2(fmaf(__uint_as_float(v0[2 * c]), a.scale_log2, -mu));
+        const float pb = ex2(fmaf(__uint_as_float(v0[2 * c + 1]), a.scale_log2, -mu));
+        const float pc = ex2(fmaf(__uint_as_float(v1[2 * c]), a.scale_log2, -mu));
+        const float pd = ex2(fmaf(__uint_as_float(v1[2 * c + 1]), a.scale_log2, -mu));
+        sum += (pa + pb) + (pc + pd);
         pk[c] = pack_bf16x2(pa, pb);
+        pk[16 + c] = pack_bf16x2(pc, pd);
       }
       l = l * factor + sum;
-      // P of page j may overwrite P of page j - 1 once O += P V for it is done
+      // Consume PV(j - 1)'s completion every page (an mbarrier parity wait is
+      // only sound one phase at a time); it is normally done by now, and O
+      // must be complete before a rescale.
       if (j >= 1) {
         ok = mbar_wait_bounded(o_done, (j - 1) & 1, a.status) && !*s_abort;
         if (!ok) break;
+        tc::fence_after();
       }
-      tc::fence_after();
       if (__any_sync(0xffffffffu, resc && j >= 1)) {
         const float f = (resc && j >= 1) ? factor : 1.f;
 #pragma unroll 1
@@ -303,7 +323,8 @@ __global__ void __launch_bounds__(192, 1)
           tc::st32(tmem + lane_base + Cfg::COL_O + c0, ov);
         }
       }
-      tc::st32(tmem + lane_base + Cfg::COL_P, pk);
+      // P over the first 32 columns of this S buffer (this warp has read them)
+      tc::st32(tmem + lane_base + Cfg::COL_S + 64 * sb, pk);
       tc::wait_st();
       // Rows of the V page past the row's frontier hold stale bytes (possibly
       // NaN); their P is 0, but 0 * NaN would still poison O, so zero them.
@@ -359,39 +380,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) tc::dealloc(tmem, Cfg::TMEM_COLS);
 }
 
-// 3-D TMA descriptor of q [B*Tc][Hq][D] (bf16): boxes of 64 dims x G heads x
-// TQ tokens = 128 rows of 128 bytes, swizzled like the K / V page tiles.
-static int encode_q_tmap(CUtensorMap* m, const void* q, int D, int Hq, int64_t rows, int G) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!fn) {
-      cudaDriverEntryPointQueryResult qr;
-      void* p = nullptr;
-      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                                       cudaEnableDefault, &qr);
-      if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !p)
-        return fail(NK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-  }
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
-                        static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
-  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(NK_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed with CUresult " + std::to_string(r));
-  return NK_OK;
-}
-
 template <int D>
-static cudaError_t launch_prefill(const CUtensorMap& tq, const nk_pool* p, int layer, const PrefillArgs& a,
-                                  dim3 grid, cudaStream_t s) {
+static cudaError_t launch_prefill(const nk_pool* p, int layer, const PrefillArgs& a, dim3 grid, cudaStream_t s) {
   using Cfg = PrefillCfg<D>;
   auto k = prefill_kernel<D>;
   static bool attr = false;
@@ -400,8 +390,7 @@ static cudaError_t launch_prefill(const CUtensorMap& tq, const nk_pool* p, int l
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, tq, p->tmap[layer * 2 + 0],
-                    p->tmap[layer * 2 + 1], a);
+  return launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, p->tmap[layer * 2 + 0], p->tmap[layer * 2 + 1], a);
 }
 
 }  // namespace nk
@@ -439,10 +428,8 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   const int G = Hq / H;
   if (G > 16 || 128 % G) return fail(NK_ERR_UNSUPPORTED, "GQA group must divide 128 and be <= 16");
   if (!aligned16(q_chunk) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
-  CUtensorMap tq;
-  int rc = encode_q_tmap(&tq, q_chunk, D, Hq, static_cast<int64_t>(B) * Tc, G);
-  if (rc) return rc;
   PrefillArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q_chunk);
   a.tables = block_tables;
   a.table_rows = table_rows;
   a.prefix_len = prefix_len;
@@ -462,8 +449,8 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   const int TQ = 128 / G;
   const dim3 grid((Tc + TQ - 1) / TQ, H, B);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = D == 256 ? launch_prefill<256>(tq, pool, layer, a, grid, s)
-                           : launch_prefill<128>(tq, pool, layer, a, grid, s);
+  cudaError_t e = D == 256 ? launch_prefill<256>(pool, layer, a, grid, s)
+                           : launch_prefill<128>(pool, layer, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return NK_OK;
 }

@@ -222,3 +222,10 @@ def test_argument_errors_launch_nothing():
     with pytest.raises(nk.NkError) as e:
         sc.gpu.decode(5, q, sc.tables_d, tr, fr, w.scale)
     assert e.value.code == -2
+
+
+def test_negative_softmax_scale():
+    """Decode with a negative softmax scale (the score order reverses)."""
+    import dataclasses
+    w = small("fp8_row", 2, 8, 128, 700, 3, 1, seed=81, contexts=[5, 300, 699])
+    run_and_check(dataclasses.replace(w, scale=-w.scale))

@@ -94,3 +94,11 @@ def test_prefill_bf16_workload_sampled():
     w = W.bf16_prefill(num_layers=1)
     sample = np.array([0, 1, 63, 64, 127, 128, 1000, 1023, 2046, 2047])
     run_prefill(w, sample_rows=sample)
+
+
+def test_prefill_negative_softmax_scale():
+    """A negative softmax scale reverses the score order; the running maximum
+    must follow the scaled scores, not the raw ones."""
+    import dataclasses
+    w = prefill_workload(2, 8, 128, 512, prefixes=[70, 0], chunks=[130, 64], Tc=192, seed=9)
+    run_prefill(dataclasses.replace(w, scale=-w.scale))
