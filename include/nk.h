@@ -128,6 +128,23 @@ int nk_pool_plane_bytes(const nk_pool_desc* desc, int32_t M, int32_t* n_planes,
  * Host only. */
 int nk_pool_capacity_bounds(const nk_pool_desc* desc, int32_t* m_min, int32_t* m_max);
 
+/* Physical pages of the MTP backend pool ("Paged KV cache" page, physical
+ * capacity of the selected speculative backend): the Main pool's M page
+ * groups plus, for each of the C active rows, the pages of its provisional
+ * lead over Main in one speculative round of draft window K:
+ *   pages = M + C * ceil((K - 1) / 64).
+ * The lead does not enlarge any row's logical capacity L.  Errors:
+ * NK_ERR_INVALID_ARG (NULL), NK_ERR_RANGE (M, C or K < 1; result > INT32_MAX). */
+int nk_pool_mtp_pages(int32_t M, int32_t C, int32_t draft_window, int32_t* pages);
+
+/* Logical pages a row keeps mapped in one pool ("Paged KV cache" page, trim of
+ * rejected speculative tails): ceil(max(committed, provisional) / 64).  The
+ * mappings of later logical blocks may be released; the last partial page is
+ * kept, and its bytes past the committed frontier are stale: no consumer reads
+ * them (every kernel stops at its frontier) and the next append at the
+ * frontier overwrites them.  Errors: NK_ERR_INVALID_ARG, NK_ERR_RANGE (< 0). */
+int nk_pages_needed(int32_t committed_frontier, int32_t provisional_frontier, int32_t* pages);
+
 /* Creates a pool handle over caller-owned planes.
  *   planes: host array of num_layers * n_planes device pointers, layer-major
  *           (planes[layer * n_planes + i]); each 16-byte aligned and at least
@@ -212,6 +229,38 @@ int nk_paged_append_decode_attention(const void* q, int32_t Hq, nk_pool* pool, i
                                      int32_t B, int32_t T, float softmax_scale, void* out,
                                      float* lse, void* workspace, size_t workspace_bytes,
                                      void* stream);
+
+/* ---- host replicas: logical-order packed pages and transfer runs ----------
+ * "Paged KV cache" page, host replica section: a host replica holds the pages
+ * of one address space in logical order, without device page ids or block
+ * table holes; each packed page holds the whole grouped payload of the pool:
+ * for layer l = 0..num_layers-1, for plane i (K code, V code, K scale, V
+ * scale), the H * 64 * row_bytes[i] bytes of that page group in plane (l, i).
+ * Transfers copy whole page payloads and merge runs of consecutive physical
+ * ids (one strided copy per run, layer and plane). */
+
+/* Bytes of one packed host page of `pool`. */
+int nk_host_page_bytes(const nk_pool* pool, size_t* bytes);
+
+/* Host helper: splits page_ids[0..n) (logical order) into runs of consecutive
+ * physical ids; run r starts at logical page run_first[r] and has run_len[r]
+ * pages.  run_first / run_len (each of n entries) may be NULL to count only.
+ * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (n < 0). */
+int nk_page_runs(const int32_t* page_ids, int32_t n, int32_t* run_first, int32_t* run_len,
+                 int32_t* n_runs);
+
+/* Copies pages page_ids[0..n) (host int32, logical order) of every layer and
+ * plane to `host` (n * nk_host_page_bytes bytes, packed as above; page-locked
+ * memory makes the copies asynchronous on `stream`).  The caller keeps the
+ * pages unchanged until the copies complete.  Errors: NK_ERR_INVALID_ARG,
+ * NK_ERR_SHAPE, NK_ERR_RANGE (an id outside [0, M); nothing is copied),
+ * NK_ERR_CUDA. */
+int nk_pages_to_host(const nk_pool* pool, const int32_t* page_ids, int32_t n, void* host, void* stream);
+
+/* The inverse: writes packed host pages into page groups page_ids[0..n) of
+ * every layer and plane (a restore may target other physical pages than the
+ * ones the replica came from).  Errors: as nk_pages_to_host. */
+int nk_pages_from_host(nk_pool* pool, const int32_t* page_ids, int32_t n, const void* host, void* stream);
 
 /* Size of the static device scratch of nk_paged_decode_attention_noalloc. */
 #define NK_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -23,8 +23,15 @@ are ordered [K code, V code, K scale, V scale]; scale planes of INT8-G64 and
 FP8-row hold IEEE binary16 (2 bytes, matching the byte table); NVFP4 scales
 are E4M3FN bytes.
 
+* speculative backends (pool geometry and trim paragraphs): the MTP pool of a
+  draft window K holds M + C * ceil((K - 1) / P) pages, the lead of each
+  active row over Main in one speculative round; a row keeps
+  ceil(max(committed, provisional) / P) logical pages mapped and may release
+  the trailing ones, the last partial page included in what it keeps.
+
 Pinned by: the byte table and the Fork/COW worked example printed on the page
-(tests/golden), the closed-form M bounds, and hand-computed addresses.
+(tests/golden), the closed-form M bounds, hand-computed addresses, and brute
+force over frontier offsets for the speculative page counts.
 """
 
 from __future__ import annotations
@@ -132,3 +139,18 @@ def fork_split(F: int) -> tuple[int, int]:
     """Fork of a frontier F: (number of full immutable pages shared,
     committed columns of the partial tail copied to a private page)."""
     return F // P, F % P
+
+
+def mtp_pages(M: int, C: int, K: int) -> int:
+    """Physical pages of the MTP backend pool for draft window K (>= 1):
+    M + C * ceil((K - 1) / P)."""
+    if K < 1:
+        raise ValueError("draft window must be >= 1")
+    return M + C * (-(-(K - 1) // P))
+
+
+def pages_needed(committed: int, provisional: int) -> int:
+    """Logical pages a row keeps mapped: ceil(max(committed, provisional) / P)."""
+    if committed < 0 or provisional < 0:
+        raise ValueError("frontiers must be >= 0")
+    return -(-max(committed, provisional) // P)

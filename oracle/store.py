@@ -14,7 +14,11 @@ Follows the "Paged KV cache" maintainer design page of the NInfer engine:
   only the oracle's way of forming the logical sequence);
 * ``copy_columns`` is the partial-tail copy-on-write of the Fork worked
   example: the committed columns of the source tail page are copied into a
-  private destination page for every plane and layer, full pages are shared.
+  private destination page for every plane and layer, full pages are shared;
+* ``pack_pages`` / ``unpack_pages`` form the host replica of the host replica
+  section: pages in logical order without device ids, each packed page holding
+  the whole grouped payload (for each layer, each plane: every (h, o) row of
+  that page group, in the plane's own (h, o) order).
 
 Parity pins: bit-exact planes against the CUDA append; invariance of gathered
 values under a random permutation of physical ids; the F = 1000 Fork example.
@@ -94,3 +98,32 @@ class PoolImage:
                     for o in range(ncols):
                         self.planes[layer][pi][self._row_slice(pi, o, h, g_dst)] = \
                             self.planes[layer][pi][self._row_slice(pi, o, h, g_src)]
+
+    # -- host replica --------------------------------------------------------
+    def packed_page_bytes(self) -> int:
+        return self.num_layers * sum(p.row_bytes * layout.P * self.H for p in self.schema)
+
+    def pack_pages(self, page_ids) -> np.ndarray:
+        """Host replica of pages page_ids (logical order): uint8 [n, page bytes]."""
+        out = []
+        for g in page_ids:
+            parts = []
+            for layer in range(self.num_layers):
+                for pi in range(len(self.schema)):
+                    for h in range(self.H):
+                        for o in range(layout.P):
+                            parts.append(self.planes[layer][pi][self._row_slice(pi, o, h, int(g))])
+            out.append(np.concatenate(parts))
+        return np.stack(out) if out else np.zeros((0, self.packed_page_bytes()), np.uint8)
+
+    def unpack_pages(self, page_ids, packed: np.ndarray) -> None:
+        """Writes a host replica back into page groups page_ids."""
+        for i, g in enumerate(page_ids):
+            at = 0
+            for layer in range(self.num_layers):
+                for pi, p in enumerate(self.schema):
+                    for h in range(self.H):
+                        for o in range(layout.P):
+                            self.planes[layer][pi][self._row_slice(pi, o, h, int(g))] = \
+                                packed[i, at:at + p.row_bytes]
+                            at += p.row_bytes

@@ -134,6 +134,26 @@ extern "C" int nk_pool_capacity_bounds(const nk_pool_desc* desc, int32_t* m_min,
   return NK_OK;
 }
 
+extern "C" int nk_pool_mtp_pages(int32_t M, int32_t C, int32_t draft_window, int32_t* pages) {
+  clear_error();
+  if (!pages) return fail(NK_ERR_INVALID_ARG, "output pointer is NULL");
+  if (M < 1 || C < 1 || draft_window < 1) return fail(NK_ERR_RANGE, "M, C and the draft window must be >= 1");
+  const int64_t lead = (static_cast<int64_t>(draft_window) - 1 + NK_PAGE_TOKENS - 1) / NK_PAGE_TOKENS;
+  const int64_t n = static_cast<int64_t>(M) + static_cast<int64_t>(C) * lead;
+  if (n > INT32_MAX) return fail(NK_ERR_RANGE, "page count does not fit int32");
+  *pages = static_cast<int32_t>(n);
+  return NK_OK;
+}
+
+extern "C" int nk_pages_needed(int32_t committed_frontier, int32_t provisional_frontier, int32_t* pages) {
+  clear_error();
+  if (!pages) return fail(NK_ERR_INVALID_ARG, "output pointer is NULL");
+  if (committed_frontier < 0 || provisional_frontier < 0) return fail(NK_ERR_RANGE, "frontiers must be >= 0");
+  const int64_t f = committed_frontier > provisional_frontier ? committed_frontier : provisional_frontier;
+  *pages = static_cast<int32_t>((f + NK_PAGE_TOKENS - 1) / NK_PAGE_TOKENS);
+  return NK_OK;
+}
+
 extern "C" int nk_pool_plane_bytes(const nk_pool_desc* desc, int32_t M, int32_t* n_planes,
                                    size_t bytes[4], size_t row_bytes[4]) {
   clear_error();

@@ -26,11 +26,13 @@ PROFILES = {"bf16": 0, "int8_g64": 1, "fp8_row": 2, "nvfp4_g16": 3, "k8v4": 4}
 POOL_CHECK_BOUNDS = 1
 
 SYMBOLS = ["nk_version", "nk_last_error", "nk_pool_plane_bytes", "nk_pool_capacity_bounds",
+           "nk_pool_mtp_pages", "nk_pages_needed",
            "nk_pool_create", "nk_pool_destroy", "nk_paged_kv_append", "nk_decode_workspace_bytes",
            "nk_paged_decode_attention", "nk_paged_append_decode_attention",
            "nk_paged_decode_attention_noalloc",
            "nk_prefill_workspace_bytes", "nk_paged_prefill_attention",
-           "nk_page_copy_columns", "nk_status_read"]
+           "nk_page_copy_columns", "nk_status_read", "nk_host_page_bytes", "nk_page_runs",
+           "nk_pages_to_host", "nk_pages_from_host"]
 
 
 class NkError(RuntimeError):
@@ -66,6 +68,12 @@ def load(path: str | None = None) -> C.CDLL:
         "nk_pool_create": (C.c_int, [C.POINTER(PoolDesc), _I, C.POINTER(_P), C.POINTER(_P)]),
         "nk_pool_destroy": (C.c_int, [_P]),
         "nk_paged_kv_append": (C.c_int, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
+        "nk_pool_mtp_pages": (C.c_int, [_I, _I, _I, C.POINTER(_I)]),
+        "nk_pages_needed": (C.c_int, [_I, _I, C.POINTER(_I)]),
+        "nk_host_page_bytes": (C.c_int, [_P, C.POINTER(_S)]),
+        "nk_page_runs": (C.c_int, [_P, _I, _P, _P, C.POINTER(_I)]),
+        "nk_pages_to_host": (C.c_int, [_P, _P, _I, _P, _P]),
+        "nk_pages_from_host": (C.c_int, [_P, _P, _I, _P, _P]),
         "nk_decode_workspace_bytes": (C.c_int, [_P, _I, _I, _I, C.POINTER(_S)]),
         "nk_paged_decode_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
         "nk_paged_append_decode_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _P, _P, _I, _I, _F, _P, _P, _P,
@@ -128,6 +136,30 @@ def nk_pool_destroy(pool: int) -> None:
 def nk_paged_kv_append(pool, layer, block_tables, table_rows, write_pos, counts, k, v, B, T, stream):
     _check(load().nk_paged_kv_append(pool, layer, block_tables, table_rows, write_pos, counts,
                                      k, v, B, T, stream))
+
+
+def nk_pool_mtp_pages(M, C_rows, draft_window) -> int:
+    n = _I()
+    _check(load().nk_pool_mtp_pages(M, C_rows, draft_window, C.byref(n)))
+    return n.value
+
+
+def nk_pages_needed(committed_frontier, provisional_frontier) -> int:
+    n = _I()
+    _check(load().nk_pages_needed(committed_frontier, provisional_frontier, C.byref(n)))
+    return n.value
+
+
+def nk_page_runs(page_ids):
+    """Runs of consecutive physical ids: list of (first logical page, length)."""
+    import numpy as np
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    n = ids.size
+    first = np.zeros(max(n, 1), np.int32)
+    ln = np.zeros(max(n, 1), np.int32)
+    nr = _I()
+    _check(load().nk_page_runs(ids.ctypes.data, n, first.ctypes.data, ln.ctypes.data, C.byref(nr)))
+    return [(int(first[r]), int(ln[r])) for r in range(nr.value)]
 
 
 def nk_decode_workspace_bytes(pool, B, T, Hq) -> int:
@@ -268,6 +300,26 @@ class Pool:
                                          _ptr(frontiers), _ptr(k), _ptr(v), B, T, float(scale), _ptr(out),
                                          _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
         return out, lse
+
+    def host_page_bytes(self) -> int:
+        n = _S()
+        _check(load().nk_host_page_bytes(self.handle, C.byref(n)))
+        return n.value
+
+    def pages_to_host(self, page_ids, host, stream=None):
+        """Packs pages page_ids (logical order) into the uint8 host tensor
+        `host` [n, host_page_bytes] (asynchronous when it is pinned)."""
+        import numpy as np
+        ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+        _check(load().nk_pages_to_host(self.handle, ids.ctypes.data, ids.size, host.data_ptr(),
+                                       _stream(stream)))
+        return host
+
+    def pages_from_host(self, page_ids, host, stream=None):
+        import numpy as np
+        ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+        _check(load().nk_pages_from_host(self.handle, ids.ctypes.data, ids.size, host.data_ptr(),
+                                         _stream(stream)))
 
     def prefill(self, layer, q, tables, table_rows, prefix_len, chunk_len, scale, out=None,
                 lse=None, workspace=None, stream=None):

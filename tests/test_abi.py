@@ -84,3 +84,34 @@ def test_host_argument_errors(lib):
                                          None, None, None, 0, None) == -1
     assert lib.nk_page_copy_columns(None, 0, 1, 4, None) == -1
     assert lib.nk_last_error()
+
+
+def test_speculative_page_geometry_matches_oracle():
+    """nk_pool_mtp_pages and nk_pages_needed are host arithmetic: checked
+    against the oracle without a GPU, including their range errors."""
+    from oracle import layout
+    for M, Cr, K in [(1, 1, 1), (512, 8, 4), (512, 8, 65), (16384, 8, 129), (4096, 2, 200)]:
+        assert nk.nk_pool_mtp_pages(M, Cr, K) == layout.mtp_pages(M, Cr, K)
+    for c, p_ in [(0, 0), (1, 0), (64, 64), (65, 3), (1000, 1004), (4092, 4096)]:
+        assert nk.nk_pages_needed(c, p_) == layout.pages_needed(c, p_)
+    with pytest.raises(nk.NkError):
+        nk.nk_pool_mtp_pages(512, 8, 0)
+    with pytest.raises(nk.NkError):
+        nk.nk_pages_needed(-1, 5)
+
+
+def test_page_runs_merge_consecutive_physical_ids():
+    """nk_page_runs (host code): runs of ids that increase by one in logical
+    order, against a plain loop."""
+    import numpy as np
+    rng = np.random.default_rng(3)
+    cases = [[], [7], [3, 4, 5, 9, 10, 2], list(range(20)), [5, 4, 3], rng.permutation(40).tolist(),
+             [0, 1, 1, 2]]
+    for ids in cases:
+        want = []
+        for i, g in enumerate(ids):
+            if want and g == ids[want[-1][0]] + want[-1][1]:
+                want[-1] = (want[-1][0], want[-1][1] + 1)
+            else:
+                want.append((i, 1))
+        assert nk.nk_page_runs(ids) == want

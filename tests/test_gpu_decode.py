@@ -229,3 +229,51 @@ def test_negative_softmax_scale():
     import dataclasses
     w = small("fp8_row", 2, 8, 128, 700, 3, 1, seed=81, contexts=[5, 300, 699])
     run_and_check(dataclasses.replace(w, scale=-w.scale))
+
+
+@pytest.mark.parametrize("profile", ["int8_g64", "k8v4", "bf16"])
+def test_rejected_speculative_tail_is_never_read_and_is_overwritten(profile):
+    """Rollback of a speculative round.  A 4-token verify (fused call) writes
+    and attends 4 provisional tokens; only the first is accepted, so the
+    committed frontier is context + 1 and the 3 rejected tokens stay in the
+    page.  Their bytes are then poisoned (0xFF) on the GPU only.  The next
+    decode appends one token at the committed frontier and attends up to it:
+    the result matches the oracle (which never holds the poison), and the
+    codes of the rewritten position are bit-exact."""
+    import dataclasses
+    w4 = small(profile, 2, 8, 128, 1024, 3, 4, seed=91, contexts=[60, 126, 500])
+    sc = Scenario(w4)
+    q, out, lse, fr = sc.step(0, fused=True)
+    ref_out, ref_lse = sc.oracle_decode(0, q, fr)
+    compare_attention(out, lse, ref_out, ref_lse)
+    committed = (w4.context + 1).astype(np.int32)
+
+    def rows_at(pos_of_b):
+        """(gpu, oracle) bytes of every plane at one position per row."""
+        got, want = [], []
+        for b in range(w4.B):
+            pos = int(pos_of_b[b])
+            g = int(w4.tables[w4.table_rows[b], pos // 64])
+            for i, plane in enumerate(sc.gpu.planes[0]):
+                rb = sc.gpu.row_bytes[i]
+                for h in range(w4.Hkv):
+                    off = ((g * w4.Hkv + h) * 64 + pos % 64) * rb
+                    got.append(plane[off:off + rb].cpu().numpy())
+                    want.append(sc.orc.planes[0][i][off:off + rb])
+        return np.concatenate(got), np.concatenate(want)
+
+    for b in range(w4.B):                       # poison the rejected tail on the GPU
+        for pos in range(int(committed[b]), int(fr[b])):
+            g = int(w4.tables[w4.table_rows[b], pos // 64])
+            for i, plane in enumerate(sc.gpu.planes[0]):
+                rb = sc.gpu.row_bytes[i]
+                for h in range(w4.Hkv):
+                    off = ((g * w4.Hkv + h) * 64 + pos % 64) * rb
+                    plane[off:off + rb] = 0xFF
+    sc.w = dataclasses.replace(w4, T=1, context=committed, seed=w4.seed + 1)
+    q1, out1, lse1, fr1 = sc.step(0, fused=True)
+    assert np.array_equal(fr1, committed + 1)
+    ref_out1, ref_lse1 = sc.oracle_decode(0, q1, fr1)
+    compare_attention(out1, lse1, ref_out1, ref_lse1)
+    got, want = rows_at(committed)
+    assert np.array_equal(got, want), "rewritten position differs from the oracle"

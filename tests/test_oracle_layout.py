@@ -148,3 +148,77 @@ def test_shared_prefix_fork_reads_identically():
 def PoolImage_gather_direct(profile, bits):
     from oracle import codec
     return codec.decode_kv(profile, codec.encode_kv(profile, bits, bits))
+
+
+# ------------------------------------------------ speculative page geometry
+
+def test_pages_needed_counts_the_touched_pages():
+    """ceil(max(committed, provisional) / P) equals the number of distinct
+    pages that positions [0, max) touch (brute force)."""
+    for c in range(0, 300, 7):
+        for p_ in range(0, 300, 11):
+            touched = len({pos >> 6 for pos in range(max(c, p_))})
+            assert layout.pages_needed(c, p_) == touched
+
+
+def test_mtp_pool_covers_the_worst_provisional_lead():
+    """The MTP pool's extra pages per row equal the largest number of pages a
+    lead of K - 1 provisional tokens can add beyond Main's membership, over
+    every committed frontier offset (brute force over a few pages)."""
+    for K in range(1, 200):
+        worst = max(layout.pages_needed(f, f + K - 1) - layout.pages_needed(f, f) for f in range(0, 4 * 64))
+        for M, C in [(1, 1), (512, 8), (16384, 8)]:
+            assert layout.mtp_pages(M, C, K) == M + C * worst
+    assert layout.mtp_pages(512, 8, 1) == 512            # no draft lead, no extra page
+    assert layout.mtp_pages(512, 8, 65) == 512 + 8        # a 64-token lead fits one page
+    assert layout.mtp_pages(512, 8, 66) == 512 + 16
+
+
+# ------------------------------------------------------------ host replica
+
+def _filled_image(profile, layers=2, H=2, D=64, M=6, seed=5):
+    from oracle.store import PoolImage
+    rng = np.random.default_rng(seed)
+    img = PoolImage(profile, layers, H, D, M)
+    for layer in range(layers):
+        for pi in range(len(img.schema)):
+            img.planes[layer][pi][:] = rng.integers(0, 256, img.planes[layer][pi].size, dtype=np.uint8)
+    return img
+
+
+@pytest.mark.parametrize("profile", ["bf16", "int8_g64", "k8v4"])
+def test_packed_page_is_the_page_major_slice_of_every_plane(profile):
+    """In the page-major order one page group is one contiguous byte range of
+    each plane, so a packed page is those ranges concatenated (layer-major,
+    then plane order) -- checked by plain slicing, not by row addressing."""
+    img = _filled_image(profile)
+    ids = [4, 0, 5, 2]
+    packed = img.pack_pages(ids)
+    for i, g in enumerate(ids):
+        expect = []
+        for layer in range(img.num_layers):
+            for pi, p in enumerate(img.schema):
+                n = p.row_bytes * 64 * img.H
+                expect.append(img.planes[layer][pi][g * n:(g + 1) * n])
+        assert np.array_equal(packed[i], np.concatenate(expect))
+
+
+def test_packed_page_size_matches_the_page_byte_table():
+    """Packed page bytes = layers x PageBytes (sum over planes of bytes per
+    token-head x 64 x H), the page's PageBytes definition."""
+    from oracle.store import PoolImage
+    for profile in layout.PROFILES:
+        img = PoolImage(profile, 3, 2, 256, 4)
+        assert img.packed_page_bytes() == layout.page_bytes(profile, 256, 2, 3)
+
+
+def test_unpack_into_other_pages_reads_the_same_logical_content():
+    """A replica restored into different physical page groups, with the
+    table row remapped, gathers to the same logical values."""
+    from oracle.store import PoolImage
+    img = _filled_image("fp8_row", layers=1, H=2, D=64, M=8)
+    src = np.array([3, 1, 6], np.int32)
+    dst = np.array([0, 7, 2], np.int32)
+    img.unpack_pages(dst, img.pack_pages(src))
+    r1, r2 = img.read_rows(0, src, 3 * 64), img.read_rows(0, dst, 3 * 64)
+    assert all(np.array_equal(r1[k], r2[k]) for k in r1)
