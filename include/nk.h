@@ -291,7 +291,9 @@ int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* 
 int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32_t Hq,
                                size_t* bytes);
 
-/* Chunked prefill / replay attention through the block tables (BF16 pools).
+/* Chunked prefill / replay attention through the block tables (BF16, FP8-row,
+ * NVFP4-G16 and K8V4 pools; quantized pages are dequantized inside the
+ * kernel, with f16 tensor-core operands that hold the codes exactly).
  * Query i < chunk_len[b] of row b sits at logical position prefix_len[b] + i
  * and attends keys j <= prefix_len[b] + i; the chunk's own K/V must already
  * be appended.  Prefill work is proportional to prefix*S + S(S+1)/2 query-key
@@ -299,7 +301,10 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
  *   q_chunk: device bf16 [B][Tc][Hq][D];  out: device bf16 [B][Tc][Hq][D]
  *   (rows i >= chunk_len[b] are not written);  lse: device fp32 [B][Tc][Hq]
  *   or NULL;  prefix_len, chunk_len: device int32 [B], chunk_len[b] <= Tc.
- * Errors as for decode; NK_ERR_UNSUPPORTED for non-BF16 pools or D != 256,128. */
+ * Errors as for decode; NK_ERR_UNSUPPORTED for INT8-G64 pools (their group
+ * products are not exact in f16 and per-group accumulators do not fit the
+ * tensor memory), for D other than 128 and 256, or a GQA group that does not
+ * divide 128 or exceeds 16. */
 int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const nk_pool* pool,
                                int32_t layer, const int32_t* block_tables,
                                const int32_t* table_rows, const int32_t* prefix_len,

@@ -56,4 +56,8 @@ int device_sm_count(int device);
 // Device address of the status word on the current device (nullptr on error).
 int* status_word();
 
+// 2-D TMA descriptor over `rows` rows of `row_bytes` bytes (viewed as uint8):
+// boxes of 64 rows x min(row_bytes, 128) bytes with the matching swizzle.
+int encode_code_tmap(CUtensorMap* m, void* base, int row_bytes, int64_t rows);
+
 }  // namespace nk

@@ -176,8 +176,11 @@ extern "C" int nk_pool_plane_bytes(const nk_pool_desc* desc, int32_t M, int32_t*
 // TMA descriptor of one code plane: a 2-D uint8 tensor of rows of row_bytes
 // bytes (one row per (g, h, o) token), boxes of 64 rows x min(row_bytes, 128)
 // bytes, swizzled so that rows of a box land in distinct shared-memory banks.
-static int encode_code_tmap(CUtensorMap* m, void* base, int row_bytes, int64_t rows) {
+namespace nk {
+int encode_code_tmap(CUtensorMap* m, void* base, int row_bytes, int64_t rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
     void* p = nullptr;
@@ -202,6 +205,7 @@ static int encode_code_tmap(CUtensorMap* m, void* base, int row_bytes, int64_t r
     return fail(NK_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return NK_OK;
 }
+}  // namespace nk
 
 extern "C" int nk_pool_create(const nk_pool_desc* desc, int32_t M, void* const* planes,
                               nk_pool** out) {

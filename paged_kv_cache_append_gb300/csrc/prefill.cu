@@ -395,13 +395,22 @@ static cudaError_t launch_prefill(const nk_pool* p, int layer, const PrefillArgs
 
 }  // namespace nk
 
+namespace nk {
+int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* tables, const int32_t* table_rows,
+                    const int32_t* prefix_len, const int32_t* chunk_len, int B, int Tc, int Hq, float scale_log2,
+                    void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t qprefill_workspace_bytes(const nk_pool* p, int B);
+}  // namespace nk
+
 using namespace nk;
 
 extern "C" int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32_t Hq,
                                           size_t* bytes) {
   clear_error();
   if (!pool || !bytes) return fail(NK_ERR_INVALID_ARG, "null argument");
-  *bytes = 0;  // the tcgen05 prefill keeps everything in shared memory and TMEM
+  // BF16 pools: none (everything stays in shared memory and TMEM); quantized
+  // pools: the f16 scratch of the dequant pass
+  *bytes = qprefill_workspace_bytes(pool, B);
   return NK_OK;
 }
 
@@ -412,13 +421,11 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
                                           float softmax_scale, void* out, float* lse,
                                           void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  (void)workspace;
-  (void)workspace_bytes;
   if (!q_chunk || !pool || !block_tables || !table_rows || !prefix_len || !chunk_len || !out)
     return fail(NK_ERR_INVALID_ARG, "null argument to nk_paged_prefill_attention");
   if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
-  if (pool->desc.profile != NK_BF16)
-    return fail(NK_ERR_UNSUPPORTED, "chunked prefill is built for BF16 pools");
+  if (pool->desc.profile == NK_INT8_G64)
+    return fail(NK_ERR_UNSUPPORTED, "chunked prefill is built for BF16, FP8-row, NVFP4-G16 and K8V4 pools");
   const int D = pool->desc.head_dim, H = pool->desc.num_kv_heads;
   if (D != 128 && D != 256) return fail(NK_ERR_UNSUPPORTED, "chunked prefill needs head_dim 128 or 256");
   if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
@@ -428,6 +435,10 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   const int G = Hq / H;
   if (G > 16 || 128 % G) return fail(NK_ERR_UNSUPPORTED, "GQA group must divide 128 and be <= 16");
   if (!aligned16(q_chunk) || !aligned16(out)) return fail(NK_ERR_ALIGN, "q / out must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pool->desc.profile != NK_BF16)
+    return qprefill_launch(pool, layer, q_chunk, block_tables, table_rows, prefix_len, chunk_len, B, Tc, Hq,
+                           softmax_scale * 1.4426950408889634f, out, lse, workspace, workspace_bytes, s);
   PrefillArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q_chunk);
   a.tables = block_tables;
@@ -448,7 +459,6 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   a.C = pool->desc.max_concurrency;
   const int TQ = 128 / G;
   const dim3 grid((Tc + TQ - 1) / TQ, H, B);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = D == 256 ? launch_prefill<256>(pool, layer, a, grid, s)
                            : launch_prefill<128>(pool, layer, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -182,7 +182,9 @@ def k8v4_long(T: int = 1, num_layers: int = 16, C: int = 8, S: int = 131072) -> 
 
 
 def bf16_prefill(num_layers: int = 16, S: int = 32768, Tc: int = 2048, decode_ctx: int = 8192,
-                 n_prefill: int = 2, n_decode: int = 6) -> Workload:
+                 n_prefill: int = 2, n_decode: int = 6, profile: str = "bf16") -> Workload:
+    """The chunked-prefill workload; `profile` other than bf16 gives the same
+    shapes over quantized pages (same seeds, so the same bf16 inputs)."""
     C = n_prefill + n_decode
     L = -(-S // P)
     M = 4096 if (S, C) == (32768, 8) else C * L
@@ -190,7 +192,8 @@ def bf16_prefill(num_layers: int = 16, S: int = 32768, Tc: int = 2048, decode_ct
     tables = _perm(5, M)[:C * L].reshape(C, L)
     r = rng.integers(1, P, n_prefill)
     prefix = (S - Tc - P + r).astype(np.int32)                # mid-page prefix
-    return Workload("bf16_prefill", "bf16", num_layers, 16, 2, 256, S, C, M, tables,
+    name = "bf16_prefill" if profile == "bf16" else f"{profile.split('_')[0]}_prefill"
+    return Workload(name, profile, num_layers, 16, 2, 256, S, C, M, tables,
                     table_rows=np.arange(n_prefill, C, dtype=np.int32),
                     context=np.full(n_decode, decode_ctx - 1, np.int32),
                     prefill_rows=np.arange(n_prefill, dtype=np.int32), prefix_len=prefix,

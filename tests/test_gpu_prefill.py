@@ -17,14 +17,14 @@ from tests.scenario import Scenario, compare_attention
 pytestmark = pytest.mark.gpu
 
 
-def prefill_workload(Hkv, G, D, S, prefixes, chunks, Tc, seed, n_decode=0, layers=1):
+def prefill_workload(Hkv, G, D, S, prefixes, chunks, Tc, seed, n_decode=0, layers=1, profile="bf16"):
     rng = np.random.default_rng(seed)
     C = len(prefixes) + n_decode
     L = -(-S // 64)
     M = C * L
     tables = rng.permutation(M).astype(np.int32).reshape(C, L)
     Bp = len(prefixes)
-    return W.Workload("prefill_test", "bf16", layers, Hkv * G, Hkv, D, S, C, M, tables,
+    return W.Workload("prefill_test", profile, layers, Hkv * G, Hkv, D, S, C, M, tables,
                       table_rows=np.arange(Bp, C, dtype=np.int32),
                       context=np.full(n_decode, 10, np.int32),
                       prefill_rows=np.arange(Bp, dtype=np.int32),
@@ -102,3 +102,47 @@ def test_prefill_negative_softmax_scale():
     import dataclasses
     w = prefill_workload(2, 8, 128, 512, prefixes=[70, 0], chunks=[130, 64], Tc=192, seed=9)
     run_prefill(dataclasses.replace(w, scale=-w.scale))
+
+
+@pytest.mark.parametrize("profile", ["fp8_row", "nvfp4_g16", "k8v4"])
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("G", [8, 1, 16])
+def test_quantized_prefill_small(profile, D, G):
+    """Prefill over FP8-row, NVFP4-G16 and K8V4 pages: a mid-page prefix and a
+    ragged chunk spanning several tiles, an empty prefix in the other row."""
+    w = prefill_workload(2 if G < 16 else 1, G, D, 1024, prefixes=[133, 0], chunks=[300, 77], Tc=320,
+                         seed=D + G + 3, profile=profile)
+    run_prefill(w)
+
+
+@pytest.mark.parametrize("profile", ["fp8_row", "k8v4"])
+def test_quantized_prefill_stale_tail_is_not_read(profile):
+    w = prefill_workload(2, 8, 256, 1024, prefixes=[100, 37], chunks=[45, 200], Tc=256, seed=15,
+                         profile=profile)
+    run_prefill(w, poison=True)
+
+
+def test_quantized_prefill_negative_scale():
+    import dataclasses
+    w = prefill_workload(2, 8, 128, 512, prefixes=[70, 0], chunks=[130, 64], Tc=192, seed=19,
+                         profile="k8v4")
+    run_prefill(dataclasses.replace(w, scale=-w.scale))
+
+
+def test_int8_prefill_is_rejected():
+    from paged_kv_cache_append_gb300 import nk
+    w = prefill_workload(2, 8, 128, 512, prefixes=[10], chunks=[20], Tc=32, seed=1, profile="int8_g64")
+    sc = Scenario(w, layers=(0,), oracle=False)
+    dev = "cuda"
+    with pytest.raises(nk.NkError):
+        sc.gpu.prefill(0, w.chunk_q(0).to(dev), sc.tables_d, torch.from_numpy(w.prefill_rows).to(dev),
+                       torch.from_numpy(w.prefix_len).to(dev), torch.from_numpy(w.chunk_len).to(dev), w.scale)
+
+
+def test_prefill_k8v4_workload_sampled():
+    """The chunked-prefill workload over K8V4 pages at full size, one layer:
+    2 rows, a 2048-token chunk after a mid-page prefix of ~30.7k tokens;
+    sampled query rows against the oracle."""
+    w = W.bf16_prefill(num_layers=1, profile="k8v4")
+    sample = np.array([0, 1, 63, 64, 127, 128, 1000, 1023, 2046, 2047])
+    run_prefill(w, sample_rows=sample)
