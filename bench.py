@@ -104,6 +104,43 @@ def workload_desc(w):
             f"{int(w.context.max()) + w.T}")
 
 
+# ------------------------------------------------------------ ranks
+
+def init_ranks(world):
+    """One process per GPU (replicas): NCCL where CUDA is present, gloo
+    otherwise; the rendezvous comes from the torchrun environment."""
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """The largest of every rank's value (the slowest replica sets the
+    step time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, ms, world):
+    """Whole-job throughput: every rank's units over the slowest rank's time
+    (weak scaling: the per-rank work is fixed)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------ clock sampler
 
 class Clocks:
@@ -362,8 +399,7 @@ def run_gpu(args, rank, world):
     # ---- timed region: K steps, L2 flushed before each --------------------
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as clk:
         t_wall = time.perf_counter()
@@ -374,14 +410,9 @@ def run_gpu(args, rank, world):
             e1.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
     clocks = clk.summary()
 
     # ---- dominant kernel: one (append +) decode launch, per layer ------------
@@ -497,8 +528,9 @@ def run_gpu(args, rank, world):
             del bc
 
     roof_kernel = "nk_paged_append_decode_attention" if bench.fused else "nk_paged_decode_attention"
-    value = world * bench.bytes_step() / (ms * 1e-3) / 1e9
-    e2e_val = world * bench.bytes_step() / (e2e_ms * 1e-3) / 1e9
+    value = job_value(bench.bytes_step(), ms, world) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_val = job_value(bench.bytes_step(), e2e_ms, world) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -519,7 +551,7 @@ def run_gpu(args, rank, world):
                    "graph": "one CUDA graph per step",
                    "step": ("fused append + decode launch per layer" if bench.fused
                             else "append launch + decode launch per layer")},
-        "rows_per_s": round(bench.B * w.T / (ms * 1e-3), 1),
+        "rows_per_s": round(world * bench.B * w.T / (ms * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
@@ -649,9 +681,7 @@ def main():
             return
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    init_ranks(world)
     line = run_gpu(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
