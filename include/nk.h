@@ -222,7 +222,13 @@ int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, in
  *   k, v: device bf16 [B][T][H][D] (16-byte aligned); other arguments and
  *   the workspace contract as in nk_paged_decode_attention.
  * A row with F_b < T is rejected on the device (status NK_STATUS_FRONTIER,
- * nothing written, out = 0, lse = -inf).  Errors: as nk_paged_decode_attention. */
+ * nothing written, out = 0, lse = -inf).
+ * Ordering: launched with programmatic stream serialization, the call reads
+ * the block tables, table_rows, frontiers and the pool pages of earlier tokens
+ * before it waits for the previous kernel in the stream (it overlaps that
+ * kernel's tail); only q, k and v may be produced by that kernel.  After a
+ * separate nk_paged_kv_append into the same rows, use nk_paged_decode_attention.
+ * Errors: as nk_paged_decode_attention. */
 int nk_paged_append_decode_attention(const void* q, int32_t Hq, nk_pool* pool, int32_t layer,
                                      const int32_t* block_tables, const int32_t* table_rows,
                                      const int32_t* frontiers, const void* k, const void* v,

@@ -221,8 +221,15 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     prefetch_tmap(&tmv);
   }
   // Launched with programmatic stream serialization: everything above overlaps
-  // the previous kernel's tail; nothing it wrote is read before this point.
-  griddep_wait();
+  // the previous kernel's tail; nothing it wrote is read before the wait.
+  // The fused call's contract leaves only q and the new k / v to the previous
+  // kernel (block tables, row map, frontiers and the pages of earlier tokens
+  // are complete before it), so there the split plan and the page loads start
+  // at once and only the consumers wait, before they read q, k or v and before
+  // any global write.  The plain decode waits here (a separate append may have
+  // just written its pages).
+  const bool early = a.k_new != nullptr;
+  if (!early) griddep_wait();
   griddep_launch_dependents();
 
   // ---- per-row lengths, loaded once in parallel ------------------------------
@@ -309,6 +316,8 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     }
     return;  // the copies complete into the shared memory of the still-running CTA
   }
+
+  if (early) griddep_wait();  // consumers: q, k, v and all writes come after the previous kernel
 
   // ---- fused append: the new tokens whose pages this CTA reads ------------------
   // One consumer warp per token encodes its K and V rows of head h into the
