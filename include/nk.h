@@ -307,6 +307,10 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
  *   q_chunk: device bf16 [B][Tc][Hq][D];  out: device bf16 [B][Tc][Hq][D]
  *   (rows i >= chunk_len[b] are not written);  lse: device fp32 [B][Tc][Hq]
  *   or NULL;  prefix_len, chunk_len: device int32 [B], chunk_len[b] <= Tc.
+ *   workspace: nk_prefill_workspace_bytes bytes, zero-filled before its first
+ *   use (every call leaves its counters at zero): the dequant scratch of
+ *   quantized pools and, when the launch splits each 128-row tile over its
+ *   pages to fill the last wave of SMs, the split partials and counters.
  * Errors as for decode; NK_ERR_UNSUPPORTED for INT8-G64 pools (their group
  * products are not exact in f16 and per-group accumulators do not fit the
  * tensor memory), for D other than 128 and 256, or a GQA group that does not

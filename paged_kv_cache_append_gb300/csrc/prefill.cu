@@ -36,6 +36,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "prefill_split.cuh"
 #include "tcgen05.cuh"
 
 namespace nk {
@@ -51,6 +52,7 @@ struct PrefillArgs {
   int* status;
   float scale_log2;  // softmax_scale * log2(e)
   int B, Tc, Hq, H, G, L, M, C;
+  PrefillSplit sp;
 };
 
 template <int D>
@@ -97,9 +99,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = q_ready + 1;     // [1]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* s_last = s_abort + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qt = blockIdx.x / a.sp.nsplit, split = blockIdx.x % a.sp.nsplit;
+  const int h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, TQ = 128 / G;
   griddep_wait();  // launched with programmatic stream serialization
   griddep_launch_dependents();
@@ -115,8 +119,12 @@ __global__ void __launch_bounds__(192, 1)
   const int t0 = qt * TQ;
   if (t0 >= chunk) return;  // no query of this tile is in the chunk
   const int t_last = min(t0 + TQ, chunk) - 1;
-  const int nkt = (prefix + t_last + 1 + 63) / 64;  // key pages to visit
-  const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L;
+  const int nkt = (prefix + t_last + 1 + 63) / 64;  // key pages of the tile
+  // this split's pages [p_lo, p_lo + n); local page i is absolute page p_lo + i
+  const int per = (nkt + a.sp.nsplit - 1) / a.sp.nsplit;
+  const int p_lo = min(split * per, nkt);
+  const int n = min(p_lo + per, nkt) - p_lo;
+  const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L + p_lo;
 
   if (tid == 0) {
     for (int i = 0; i < NK; ++i) {
@@ -150,8 +158,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     int gnext = 0;
-    for (int j = 0; j < nkt; ++j) {
-      if ((j & 31) == 0) gnext = (j + lane < nkt) ? table[j + lane] : 0;
+    for (int j = 0; j < n; ++j) {
+      if ((j & 31) == 0) gnext = (j + lane < n) ? table[j + lane] : 0;
       int g = __shfl_sync(0xffffffffu, gnext, j & 31);
       int stop = 0;
       if (lane == 0) {
@@ -184,8 +192,8 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       bool ok = mbar_wait_bounded(q_ready, 0, a.status);
       tc::fence_after();
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {  // S(j) = Q K(j)^T into buffer j & 1
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {  // S(j) = Q K(j)^T into buffer j & 1
           const int ks = j % NK, sb = j & 1;
           ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status);
           if (!ok) break;
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool pos_scale = a.scale_log2 >= 0.f;
     const float fill = pos_scale ? -INFINITY : INFINITY;
     bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
+    for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
       ok = mbar_wait_bounded(&s_full[sb], (j / 2) & 1, a.status) && !*s_abort;
       if (!ok) break;
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(192, 1)
       // raw score (the smallest one for a negative scale); masked keys get the
       // fill value that no extremum picks and whose exponent is 0.  The causal
       // mask is applied only where the page reaches past a row's last key.
-      const int kmax = row_valid ? pos - 64 * j : -1;  // keys c <= kmax of this page are visible
+      const int kmax = row_valid ? pos - 64 * (p_lo + j) : -1;  // keys c <= kmax of this page are visible
       float rext = fill;
       if (__all_sync(0xffffffffu, kmax >= 63)) {
 #pragma unroll
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(192, 1)
       tc::wait_st();
       // Rows of the V page past the row's frontier hold stale bytes (possibly
       // NaN); their P is 0, but 0 * NaN would still poison O, so zero them.
-      const int kstale = prefix + chunk - 64 * j;
+      const int kstale = prefix + chunk - 64 * (p_lo + j);
       if (kstale < 64) {
         const int vs = j % NV;
         ok = mbar_wait_bounded(&v_full[vs], (j / NV) & 1, a.status);
@@ -345,30 +353,14 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) arrive(p_full);
     }
-    // ---- epilogue: O / l to bf16 -------------------------------------------
-    if (ok) ok = mbar_wait_bounded(o_done, (nkt - 1) & 1, a.status) && !*s_abort;
+    // ---- epilogue: O / l to bf16, or this split's partial and the merge ------
+    if (ok && n > 0) ok = mbar_wait_bounded(o_done, (n - 1) & 1, a.status) && !*s_abort;
     tc::fence_after();
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        tc::ld32(tmem + lane_base + Cfg::COL_O + c0, ov);
-        tc::wait_ld();
-        if (row_valid) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + c0 + 8 * c) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-      }
-      if (row_valid && a.lse)
-        a.lse[(static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g] =
-            l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const int64_t orow = (static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g;
+      const int64_t tile = (static_cast<int64_t>(b) * a.H + h) * a.sp.tiles + qt;
+      prefill_store<D>(tmem + lane_base + Cfg::COL_O, n > 0, row_valid, m_used, l, a.out + orow * D,
+                       a.lse ? a.lse + orow : nullptr, a.sp, tile, split, m, s_last);
     }
   }
 
@@ -408,9 +400,16 @@ extern "C" int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_
                                           size_t* bytes) {
   clear_error();
   if (!pool || !bytes) return fail(NK_ERR_INVALID_ARG, "null argument");
-  // BF16 pools: none (everything stays in shared memory and TMEM); quantized
-  // pools: the f16 scratch of the dequant pass
-  *bytes = qprefill_workspace_bytes(pool, B);
+  if (Hq < 1 || Hq % pool->desc.num_kv_heads || Tc < 1 || B < 1) return fail(NK_ERR_SHAPE, "bad B, Tc or Hq");
+  // quantized pools: the f16 scratch of the dequant pass; then, when the
+  // tiles are split over their pages, the partials and counters (zero-filled
+  // before the first use, left at zero by every call)
+  const int H = pool->desc.num_kv_heads, G = Hq / H;
+  if (G > 16 || 128 % G) return fail(NK_ERR_UNSUPPORTED, "GQA group must divide 128 and be <= 16");
+  const int tiles = (Tc + 128 / G - 1) / (128 / G);
+  const int nsplit = prefill_nsplit(tiles * H * B, pool->num_sms);
+  *bytes = (qprefill_workspace_bytes(pool, B) + 255) / 256 * 256 +
+           prefill_split_bytes(B, H, tiles, nsplit, pool->desc.head_dim);
   return NK_OK;
 }
 
@@ -458,7 +457,14 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   const int TQ = 128 / G;
-  const dim3 grid((Tc + TQ - 1) / TQ, H, B);
+  const int tiles = (Tc + TQ - 1) / TQ;
+  const int nsplit = prefill_nsplit(tiles * H * B, pool->num_sms);
+  const size_t need = prefill_split_bytes(B, H, tiles, nsplit, D);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(NK_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
+  if (need && !aligned16(workspace)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
+  a.sp = prefill_split_at(workspace, B, H, tiles, nsplit);
+  const dim3 grid(tiles * nsplit, H, B);
   cudaError_t e = D == 256 ? launch_prefill<256>(pool, layer, a, grid, s)
                            : launch_prefill<128>(pool, layer, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

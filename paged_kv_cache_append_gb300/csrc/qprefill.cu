@@ -36,6 +36,7 @@
 
 #include "encode.cuh"
 #include "internal.h"
+#include "prefill_split.cuh"
 #include "tcgen05.cuh"
 
 namespace nk {
@@ -73,6 +74,7 @@ struct QArgs {
   float scale_log2;  // softmax_scale * log2(e)
   float thr;         // rescale threshold in log2 units
   int B, Tc, Hq, H, G, L, M, C;
+  PrefillSplit sp;
 };
 
 // Row geometry shared by both passes; false when the row is malformed.
@@ -188,9 +190,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = q_ready + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* s_last = s_abort + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qt = blockIdx.x / a.sp.nsplit, split = blockIdx.x % a.sp.nsplit;
+  const int h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, TQ = 128 / G;
   griddep_wait();  // the dequant pass has completed
   griddep_launch_dependents();
@@ -204,7 +208,11 @@ __global__ void __launch_bounds__(192, 1)
   if (t0 >= chunk) return;
   const int t_last = min(t0 + TQ, chunk) - 1;
   const int nkt = (prefix + t_last + 1 + 63) / 64;
-  const int page0 = (b * a.H + h) * a.L;  // scratch page of logical page 0
+  // this split's pages [p_lo, p_lo + n); local page i is absolute page p_lo + i
+  const int per = (nkt + a.sp.nsplit - 1) / a.sp.nsplit;
+  const int p_lo = min(split * per, nkt);
+  const int n = min(p_lo + per, nkt) - p_lo;
+  const int page0 = (b * a.H + h) * a.L + p_lo;  // scratch page of local page 0
 
   if (tid == 0) {
     for (int i = 0; i < NK; ++i) {
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     // -------- TMA producer: f16 K / V tiles and the scales of each page --------
     if (lane == 0) {
-      for (int j = 0; j < nkt; ++j) {
+      for (int j = 0; j < n; ++j) {
         const int y = (page0 + j) * 64;
         const int ks = j % NK, vs = j % NV;
         if (j >= NK && !mbar_wait_bounded(&k_empty[ks], ((j / NK) - 1) & 1, a.status)) break;
@@ -259,8 +267,8 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       bool ok = mbar_wait_bounded(q_ready, 0, a.status);
       tc::fence_after();
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {
           const int ks = j % NK, sb = j & 1;
           ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status);
           if (!ok) break;
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
+    for (int j = 0; j < n; ++j) {
       const int sb = j & 1, vs = j % NV;
       ok = mbar_wait_bounded(&s_full[sb], (j / 2) & 1, a.status) && !*s_abort;
       // the page's scales travel with its V tile, which stays until PV(j)
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(192, 1)
       tc::wait_ld();
       const float* ksc = reinterpret_cast<const float*>(sV + vs * Cfg::V_STAGE + Cfg::KV_BYTES);
       const float* vsc = ksc + 64;
-      const int kmax = row_valid ? pos - 64 * j : -1;
+      const int kmax = row_valid ? pos - 64 * (p_lo + j) : -1;
       float rmax = -INFINITY;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
@@ -421,29 +429,13 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) q_arrive(p_full);
     }
-    if (ok) ok = mbar_wait_bounded(o_done, (nkt - 1) & 1, a.status) && !*s_abort;
+    if (ok && n > 0) ok = mbar_wait_bounded(o_done, (n - 1) & 1, a.status) && !*s_abort;
     tc::fence_after();
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        tc::ld32(tmem + lane_base + Cfg::COL_O + c0, ov);
-        tc::wait_ld();
-        if (row_valid) {
-          uint32_t o2[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            o2[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + c0 + 8 * c) = make_uint4(o2[4 * c], o2[4 * c + 1], o2[4 * c + 2], o2[4 * c + 3]);
-        }
-      }
-      if (row_valid && a.lse)
-        a.lse[(static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g] =
-            l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const int64_t orow = (static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g;
+      const int64_t tile = (static_cast<int64_t>(b) * a.H + h) * a.sp.tiles + qt;
+      prefill_store<D>(tmem + lane_base + Cfg::COL_O, n > 0, row_valid, m_used, l, a.out + orow * D,
+                       a.lse ? a.lse + orow : nullptr, a.sp, tile, split, m, s_last);
     }
   }
 
@@ -466,8 +458,7 @@ static cudaError_t launch_passes(const CUtensorMap& tk, const CUtensorMap& tv, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int TQ = 128 / a.G;
-  return launch_pdl(k, dim3((a.Tc + TQ - 1) / TQ, a.H, a.B), dim3(Cfg::THREADS), Cfg::SMEM, s, tk, tv, a);
+  return launch_pdl(k, dim3(a.sp.tiles * a.sp.nsplit, a.H, a.B), dim3(Cfg::THREADS), Cfg::SMEM, s, tk, tv, a);
 }
 
 template <int KK, int KV>
@@ -486,7 +477,10 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
                     const int32_t* prefix_len, const int32_t* chunk_len, int B, int Tc, int Hq, float scale_log2,
                     void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t s) {
   const int D = p->desc.head_dim, H = p->desc.num_kv_heads;
-  const size_t need = QScratch::bytes(B, H, p->L, D);
+  const int tiles = (Tc + 128 / (Hq / H) - 1) / (128 / (Hq / H));
+  const int nsplit = prefill_nsplit(tiles * H * B, p->num_sms);
+  const size_t scr = (QScratch::bytes(B, H, p->L, D) + 255) / 256 * 256;
+  const size_t need = scr + prefill_split_bytes(B, H, tiles, nsplit, D);
   if (!ws || ws_bytes < need) return fail(NK_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
   if (!aligned16(ws)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
   QArgs a;
@@ -514,6 +508,7 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   a.L = p->L;
   a.M = p->M;
   a.C = p->desc.max_concurrency;
+  a.sp = prefill_split_at(static_cast<char*>(ws) + scr, B, H, tiles, nsplit);
   const int64_t rows = static_cast<int64_t>(B) * H * p->L * 64;
   CUtensorMap tk, tv;
   int rc = encode_code_tmap(&tk, a.scr.k, D * 2, rows);

@@ -146,3 +146,11 @@ def test_prefill_k8v4_workload_sampled():
     w = W.bf16_prefill(num_layers=1, profile="k8v4")
     sample = np.array([0, 1, 63, 64, 127, 128, 1000, 1023, 2046, 2047])
     run_prefill(w, sample_rows=sample)
+
+
+@pytest.mark.parametrize("profile", ["bf16", "k8v4"])
+def test_prefill_without_page_splits(profile):
+    """152 tiles (one wave of 1-CTA-per-SM work) leave each tile whole
+    (no partials); the other tests run split tiles."""
+    w = prefill_workload(2, 8, 128, 1400, prefixes=[61], chunks=[1216], Tc=1216, seed=23, profile=profile)
+    run_prefill(w, sample_rows=np.array([0, 15, 16, 600, 1215]))
