@@ -210,11 +210,12 @@ class Bench:
     """Device state of one workload; `share` reuses another Bench's filled
     pool (a sub-batch of its first B rows)."""
 
-    def __init__(self, w, device, B=None, share=None, fused=True):
+    def __init__(self, w, device, B=None, share=None, fused=True, host_values=False):
         import torch
         from paged_kv_cache_append_gb300 import nk
         self.torch, self.nk, self.w, self.dev = torch, nk, w, device
         self.fused = fused
+        self.host_values = host_values   # context values drawn on the host (the oracle's stream)
         B = w.B if B is None else B
         self.B = B
         self.tables = torch.from_numpy(w.tables).to(device)
@@ -265,7 +266,7 @@ class Bench:
         ctx[w.table_rows] = w.context
         if len(w.prefill_rows):
             ctx[w.prefill_rows] = w.prefix_len
-        gen_dev = self.dev if w.S * w.C * w.Hkv * w.D > (1 << 26) else "cpu"
+        gen_dev = self.dev if (w.S * w.C * w.Hkv * w.D > (1 << 26) and not self.host_values) else "cpu"
         for layer in range(w.num_layers):
             for r in range(w.C):
                 start = sh if (sh and r > 0) else 0
