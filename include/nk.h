@@ -85,7 +85,9 @@ typedef enum {
 
 /* Plane order ("Paged KV cache" page, closed orders: page-major
  * [X, P, H, N_physical] for Main/MTP pools, head-major [X, P, N_physical, H]
- * for the draft pool).  Only page-major is built. */
+ * for the draft pool).  Both are built: a (page group g, KV head h) tile of
+ * 64 token rows starts at row (g * H + h) * 64 of a plane in page-major order
+ * and at row (h * M + g) * 64 in head-major order. */
 typedef enum { NK_PAGE_MAJOR = 0, NK_HEAD_MAJOR = 1 } nk_order;
 
 /* Pool flags.  NK_POOL_CHECK_BOUNDS is accepted for callers that ask for
@@ -101,7 +103,7 @@ typedef struct {
   int32_t head_dim;        /* D in {64, 128, 256}                            */
   int32_t max_context;     /* S >= 1                                         */
   int32_t max_concurrency; /* C in 1..8; block table has C rows of L entries */
-  int32_t order;           /* nk_order; must be NK_PAGE_MAJOR                */
+  int32_t order;           /* nk_order                                       */
   int32_t flags;           /* NK_POOL_* bits                                 */
 } nk_pool_desc;
 

@@ -30,6 +30,7 @@ struct AppendArgs {
   uint8_t* vs;  // V scale plane
   int* status;
   int B, T, H, L, M, C;
+  int head_major;  // plane order
 };
 
 template <int KK, int KV, int D>
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
     if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
     return;
   }
-  const int64_t token_row = (static_cast<int64_t>(g) * a.H + h) * 64 + (pos & 63);
+  const int64_t token_row = tile_row(g, h, a.H, a.M, a.head_major) + (pos & 63);
   const int64_t src = ((static_cast<int64_t>(b) * a.T + t) * a.H + h) * D;
 
   constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
@@ -110,6 +111,7 @@ extern "C" int nk_paged_kv_append(nk_pool* pool, int32_t layer, const int32_t* b
   a.L = pool->L;
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
+  a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = pool->desc.head_dim;
   switch (pool->desc.profile) {

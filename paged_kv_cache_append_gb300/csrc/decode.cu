@@ -112,6 +112,7 @@ static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t la
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
+  a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   if (k_new) {
     a.k_new = static_cast<const __nv_bfloat16*>(k_new);
     a.v_new = static_cast<const __nv_bfloat16*>(v_new);
@@ -207,6 +208,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
+  a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   // the scratch is shared by every call: its split counters start at zero
   cudaError_t e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(B) * H * sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the split counters");

@@ -72,6 +72,7 @@ struct DecodeArgs {
   float softmax_scale;
   int B, T, Hq, H, G, L, M, C;
   int target;    // splits per head the chunking aims at (= maxsplit)
+  int head_major = 0;  // plane order
 };
 
 template <int KIND>
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
             g = 0;                  // the row's result is then undefined
           }
           uint8_t* st = smem + s * Cfg::STAGE;
-          const int y = (g * a.H + h) * 64;
+          const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
           mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
 #pragma unroll
           for (int j = 0; j < Cfg::KCB / Cfg::K_RB; ++j)
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
         continue;
       }
-      const int64_t token_row = (static_cast<int64_t>(g) * a.H + h) * 64 + (pos & 63);
+      const int64_t token_row = tile_row(g, h, a.H, a.M, a.head_major) + (pos & 63);
       const int64_t src = ((static_cast<int64_t>(b) * a.T + t) * a.H + h) * D;
       encode_row<KK, D>(a.k_new + src, a.kc_w + token_row * KCBW, a.ks_w ? a.ks_w + token_row * KSBW : nullptr, lane);
       encode_row<KV, D>(a.v_new + src, a.vc_w + token_row * VCBW, a.vs_w ? a.vs_w + token_row * VSBW : nullptr, lane);

@@ -50,6 +50,13 @@ int plane_geoms(int profile, int D, int* n_planes, PlaneGeom g[4]);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// First row (of row_bytes each) of the 64-token tile of page group g, KV head
+// h in a plane ("Paged KV cache" page, closed plane orders): page-major
+// [X, P, H, M] gives (g * H + h) * 64, head-major [X, P, M, H] (h * M + g) * 64.
+__host__ __device__ __forceinline__ int64_t tile_row(int g, int h, int H, int M, int head_major) {
+  return head_major ? (static_cast<int64_t>(h) * M + g) * 64 : (static_cast<int64_t>(g) * H + h) * 64;
+}
+
 // Caches the SM count of a device.
 int device_sm_count(int device);
 

@@ -108,8 +108,8 @@ static int check_desc(const nk_pool_desc* d) {
     return fail(NK_ERR_SHAPE, "num_layers, num_kv_heads and max_context must be >= 1");
   if (d->max_concurrency < 1 || d->max_concurrency > 8)
     return fail(NK_ERR_SHAPE, "max_concurrency must be in 1..8");
-  if (d->order != NK_PAGE_MAJOR)
-    return fail(NK_ERR_UNSUPPORTED, "only the page-major plane order is built");
+  if (d->order != NK_PAGE_MAJOR && d->order != NK_HEAD_MAJOR)
+    return fail(NK_ERR_INVALID_ARG, "order must be NK_PAGE_MAJOR or NK_HEAD_MAJOR");
   if (d->flags & ~NK_POOL_CHECK_BOUNDS) return fail(NK_ERR_INVALID_ARG, "unknown pool flags");
   return NK_OK;
 }
@@ -282,12 +282,14 @@ extern "C" int nk_page_copy_columns(const nk_pool* pool, int32_t src, int32_t ds
   for (int l = 0; l < pool->desc.num_layers; ++l) {
     for (int i = 0; i < pool->n_planes; ++i) {
       const size_t rb = pool->plane[i].row_bytes;
-      const size_t head_pitch = rb * NK_PAGE_TOKENS;   // nb2
-      const size_t page_pitch = head_pitch * H;        // nb3
+      const int hm = pool->desc.order == NK_HEAD_MAJOR;
+      // columns [0, ncols) of every head are one contiguous run per head; the
+      // heads of a page group are tile_row(g, 1) - tile_row(g, 0) rows apart
+      const size_t head_pitch = static_cast<size_t>(tile_row(0, 1, H, pool->M, hm)) * rb;
       char* base = static_cast<char*>(pool->ptrs[l * pool->n_planes + i]);
-      // columns [0, ncols) of every head are one contiguous run per head
-      cudaError_t e = cudaMemcpy2DAsync(base + dst * page_pitch, head_pitch, base + src * page_pitch,
-                                        head_pitch, rb * ncols, H, cudaMemcpyDeviceToDevice, s);
+      cudaError_t e = cudaMemcpy2DAsync(base + tile_row(dst, 0, H, pool->M, hm) * rb, head_pitch,
+                                        base + tile_row(src, 0, H, pool->M, hm) * rb, head_pitch, rb * ncols, H,
+                                        cudaMemcpyDeviceToDevice, s);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync (page copy)");
     }
   }

@@ -53,6 +53,7 @@ struct PrefillArgs {
   float scale_log2;  // softmax_scale * log2(e)
   int B, Tc, Hq, H, G, L, M, C;
   PrefillSplit sp;
+  int head_major;  // plane order
 };
 
 template <int D>
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(192, 1)
           set_status(a.status, NK_STATUS_PAGE_RANGE);
           g = 0;
         }
-        const int y = (g * a.H + h) * 64;
+        const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
         const int ks = j % NK, vs = j % NV;
         if (j >= NK && !mbar_wait_bounded(&k_empty[ks], ((j / NK) - 1) & 1, a.status)) stop = 1;
         if (!stop) {
@@ -456,6 +457,7 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   a.L = pool->L;
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
+  a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   const int TQ = 128 / G;
   const int tiles = (Tc + TQ - 1) / TQ;
   const int nsplit = prefill_nsplit(tiles * H * B, pool->num_sms);

@@ -75,6 +75,7 @@ struct QArgs {
   float thr;         // rescale threshold in log2 units
   int B, Tc, Hq, H, G, L, M, C;
   PrefillSplit sp;
+  int head_major;  // plane order
 };
 
 // Row geometry shared by both passes; false when the row is malformed.
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(128) qdequant_kernel(QArgs a) {
   constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
   constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
   const int kvalid = g < 0 ? 0 : F - 64 * p;            // rows >= kvalid are stale: zeros
-  const int64_t src = (static_cast<int64_t>(g) * a.H + h) * 64;
+  const int64_t src = g < 0 ? 0 : tile_row(g, h, a.H, a.M, a.head_major);
   const int64_t dst = ((static_cast<int64_t>(b) * a.H + h) * a.L + p) * 64;
   for (int c = tid; c < 64 * (D / 8); c += 128) {
     const int r = c / (D / 8), d = (c % (D / 8)) * 8;
@@ -509,6 +510,7 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   a.M = p->M;
   a.C = p->desc.max_concurrency;
   a.sp = prefill_split_at(static_cast<char*>(ws) + scr, B, H, tiles, nsplit);
+  a.head_major = p->desc.order == NK_HEAD_MAJOR;
   const int64_t rows = static_cast<int64_t>(B) * H * p->L * 64;
   CUtensorMap tk, tv;
   int rc = encode_code_tmap(&tk, a.scr.k, D * 2, rows);

@@ -52,18 +52,29 @@ int copy_pages(const nk_pool* p, const int32_t* ids, int32_t n, char* host, bool
   make_runs(ids, n, first, len);
   const size_t pb = page_payload(p);
   const int H = p->desc.num_kv_heads;
+  const int hm = p->desc.order == NK_HEAD_MAJOR;
   for (size_t r = 0; r < first.size(); ++r) {
+    const int g0 = ids[first[r]];
     size_t off = 0;  // byte offset of (layer, plane) inside a packed page
     for (int l = 0; l < p->desc.num_layers; ++l) {
       for (int i = 0; i < p->n_planes; ++i) {
-        const size_t slice = p->plane[i].row_bytes * NK_PAGE_TOKENS * static_cast<size_t>(H);
-        char* dev = static_cast<char*>(p->ptrs[l * p->n_planes + i]) + static_cast<size_t>(ids[first[r]]) * slice;
+        const size_t tile = p->plane[i].row_bytes * NK_PAGE_TOKENS;  // one (page, head) tile
+        char* base = static_cast<char*>(p->ptrs[l * p->n_planes + i]);
         char* hst = host + static_cast<size_t>(first[r]) * pb + off;
-        cudaError_t e = to_host
-            ? cudaMemcpy2DAsync(hst, pb, dev, slice, slice, len[r], cudaMemcpyDeviceToHost, s)
-            : cudaMemcpy2DAsync(dev, slice, hst, pb, slice, len[r], cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, to_host ? "page run D2H" : "page run H2D");
-        off += slice;
+        // page-major: the H tiles of a page are contiguous, and so are the pages
+        // of a run (one copy); head-major: one copy per head, the run's pages
+        // of that head are contiguous
+        const int parts = hm ? H : 1;
+        const size_t width = hm ? tile : tile * H;
+        for (int hh = 0; hh < parts; ++hh) {
+          char* dev = base + static_cast<size_t>(tile_row(g0, hh, H, p->M, hm)) * p->plane[i].row_bytes;
+          char* hp = hst + hh * tile;
+          cudaError_t e = to_host
+              ? cudaMemcpy2DAsync(hp, pb, dev, width, width, len[r], cudaMemcpyDeviceToHost, s)
+              : cudaMemcpy2DAsync(dev, width, hp, pb, width, len[r], cudaMemcpyHostToDevice, s);
+          if (e != cudaSuccess) return cuda_fail(e, to_host ? "page run D2H" : "page run H2D");
+        }
+        off += tile * H;
       }
     }
   }

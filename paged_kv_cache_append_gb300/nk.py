@@ -96,10 +96,14 @@ def _check(rc: int) -> None:
         raise NkError(rc, load().nk_last_error().decode())
 
 
+ORDERS = {"page_major": 0, "head_major": 1}
+
+
 def make_desc(profile, num_layers, num_kv_heads, head_dim, max_context, max_concurrency,
-              flags: int = 0) -> PoolDesc:
+              flags: int = 0, order: str = "page_major") -> PoolDesc:
     prof = PROFILES[profile] if isinstance(profile, str) else int(profile)
-    return PoolDesc(prof, num_layers, num_kv_heads, head_dim, max_context, max_concurrency, 0, flags)
+    return PoolDesc(prof, num_layers, num_kv_heads, head_dim, max_context, max_concurrency,
+                    ORDERS[order], flags)
 
 
 # ----------------------------------------------------------- C-named wrappers
@@ -231,13 +235,14 @@ class Pool:
 
     def __init__(self, profile: str, num_layers: int, num_kv_heads: int, head_dim: int,
                  max_context: int, max_concurrency: int, M: int, device="cuda",
-                 check_bounds: bool = False):
+                 check_bounds: bool = False, order: str = "page_major"):
         import torch
         self.profile, self.num_layers, self.H, self.D = profile, num_layers, num_kv_heads, head_dim
         self.S, self.C, self.M = max_context, max_concurrency, M
         self.L = -(-max_context // 64)
+        self.order = order
         self.desc = make_desc(profile, num_layers, num_kv_heads, head_dim, max_context,
-                              max_concurrency, POOL_CHECK_BOUNDS if check_bounds else 0)
+                              max_concurrency, POOL_CHECK_BOUNDS if check_bounds else 0, order)
         self.n_planes, self.plane_bytes, self.row_bytes = nk_pool_plane_bytes(self.desc, M)
         self.planes = [[torch.zeros(nb, dtype=torch.uint8, device=device) for nb in self.plane_bytes]
                        for _ in range(num_layers)]

@@ -33,11 +33,12 @@ class Scenario:
     copy-on-write tail), one decode step per layer: append T tokens per decode
     row, then attend."""
 
-    def __init__(self, w: Workload, layers=(0,), device="cuda", oracle=True, check_bounds=False):
+    def __init__(self, w: Workload, layers=(0,), device="cuda", oracle=True, check_bounds=False,
+                 order="page_major"):
         self.w, self.layers, self.device, self.with_oracle = w, list(layers), device, oracle
         self.gpu = nk.Pool(w.profile, w.num_layers, w.Hkv, w.D, w.S, w.C, w.M, device=device,
-                           check_bounds=check_bounds)
-        self.orc = PoolImage(w.profile, w.num_layers, w.Hkv, w.D, w.M) if oracle else None
+                           check_bounds=check_bounds, order=order)
+        self.orc = PoolImage(w.profile, w.num_layers, w.Hkv, w.D, w.M, order=order) if oracle else None
         self.tables_d = torch.from_numpy(w.tables).to(device)
         self._fill()
 

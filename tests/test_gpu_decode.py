@@ -27,8 +27,8 @@ def small(profile, Hkv, G, D, S, C, T, seed, contexts=None, layers=1, outliers=T
                       outlier_p=0.01 if outliers else 0.0, outlier_mul=20.0)
 
 
-def run_and_check(w, layer=0, strict=False, fused=False):
-    sc = Scenario(w, layers=(layer,))
+def run_and_check(w, layer=0, strict=False, fused=False, order="page_major"):
+    sc = Scenario(w, layers=(layer,), order=order)
     q, out, lse, fr = sc.step(layer, fused=fused)
     bad = sc.planes_equal(layer)
     assert not bad, f"plane mismatch (plane, count, first index, gpu, oracle): {bad}"
@@ -277,3 +277,25 @@ def test_rejected_speculative_tail_is_never_read_and_is_overwritten(profile):
     compare_attention(out1, lse1, ref_out1, ref_lse1)
     got, want = rows_at(committed)
     assert np.array_equal(got, want), "rewritten position differs from the oracle"
+
+
+@pytest.mark.parametrize("profile", ["bf16", "int8_g64", "fp8_row", "nvfp4_g16", "k8v4"])
+@pytest.mark.parametrize("D,G,T", [(128, 8, 1), (256, 8, 1), (128, 2, 4)])
+@pytest.mark.parametrize("fused", [False, True], ids=["append_then_decode", "fused"])
+def test_head_major_plane_order(profile, D, G, T, fused):
+    """Pools in the head-major order [X, P, N, H] of the draft pool: the
+    append writes, and the decode reads, the same logical content as the
+    oracle's head-major image (planes bit-exact, attention within tolerance)."""
+    w = small(profile, 2, G, D, 400, 3, T, seed=D + G + T + 300, contexts=[0, 190, 400 - T])
+    run_and_check(w, fused=fused, order="head_major")
+
+
+def test_head_major_shared_prefix_with_cow_tail():
+    """Fork with a partial-tail copy (nk_page_copy_columns) in a head-major
+    pool: the per-head column runs sit M pages apart."""
+    w = W.fp8_shared(num_layers=1, C=4, S=2048, shared_len=1000)
+    sc = Scenario(w, layers=(0,), order="head_major")
+    q, out, lse, fr = sc.step(0, fused=True)
+    assert not sc.planes_equal(0)
+    ref_out, ref_lse = sc.oracle_decode(0, q, fr)
+    compare_attention(out, lse, ref_out, ref_lse)

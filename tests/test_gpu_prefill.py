@@ -32,8 +32,8 @@ def prefill_workload(Hkv, G, D, S, prefixes, chunks, Tc, seed, n_decode=0, layer
                       Tc=Tc, scale=1 / math.sqrt(D), seed=seed + 9000)
 
 
-def run_prefill(w, layer=0, poison=False, sample_rows=None):
-    sc = Scenario(w, layers=(layer,), oracle=True)
+def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major"):
+    sc = Scenario(w, layers=(layer,), oracle=True, order=order)
     dev = "cuda"
     k, v = w.chunk_kv(layer)
     q = w.chunk_q(layer)
@@ -154,3 +154,10 @@ def test_prefill_without_page_splits(profile):
     (no partials); the other tests run split tiles."""
     w = prefill_workload(2, 8, 128, 1400, prefixes=[61], chunks=[1216], Tc=1216, seed=23, profile=profile)
     run_prefill(w, sample_rows=np.array([0, 15, 16, 600, 1215]))
+
+
+@pytest.mark.parametrize("profile", ["bf16", "k8v4", "nvfp4_g16"])
+def test_prefill_head_major_plane_order(profile):
+    w = prefill_workload(2, 8, 256, 1024, prefixes=[133, 0], chunks=[300, 77], Tc=320, seed=29,
+                         profile=profile)
+    run_prefill(w, order="head_major")

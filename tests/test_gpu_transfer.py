@@ -30,9 +30,10 @@ def xfer_workload(profile, identity, seed):
 
 @pytest.mark.parametrize("profile", ["bf16", "int8_g64", "fp8_row", "nvfp4_g16", "k8v4"])
 @pytest.mark.parametrize("identity", [False, True], ids=["scattered", "consecutive"])
-def test_host_replica_round_trip(profile, identity):
+@pytest.mark.parametrize("order", ["page_major", "head_major"])
+def test_host_replica_round_trip(profile, identity, order):
     w = xfer_workload(profile, identity, seed=7 + identity)
-    sc = Scenario(w, layers=(0, 1))
+    sc = Scenario(w, layers=(0, 1), order=order)
     src = w.tables[1, :5]                 # the 5 pages of row 1 (context 300)
     runs = nk.nk_page_runs(src)
     assert (len(runs) == 1) if identity else (len(runs) >= 2)
