@@ -318,7 +318,17 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     return;  // the copies complete into the shared memory of the still-running CTA
   }
 
-  if (early) griddep_wait();  // consumers: q, k, v and all writes come after the previous kernel
+  if (early) {
+    // the q rows of this (row, KV head) and its new k / v rows into L2 while the
+    // previous kernel finishes; they are read right after the wait
+    if (tid < a.T) {
+      const int64_t bt = static_cast<int64_t>(b) * a.T + tid;
+      prefetch_l2(a.q + (bt * a.Hq + h * a.G) * D, a.G * D * 2);
+      prefetch_l2(a.k_new + (bt * a.H + h) * D, D * 2);
+      prefetch_l2(a.v_new + (bt * a.H + h) * D, D * 2);
+    }
+    griddep_wait();  // consumers: q, k, v and all writes come after the previous kernel
+  }
 
   // ---- fused append: the new tokens whose pages this CTA reads ------------------
   // One consumer warp per token encodes its K and V rows of head h into the

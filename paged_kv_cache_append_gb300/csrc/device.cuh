@@ -106,6 +106,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 
 // ------------------------------------------------------------ async copies
 
+// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address.  L2
+// is the point of coherence, so a prefetch issued before a dependency wait
+// cannot make a later load return stale data.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
