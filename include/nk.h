@@ -195,15 +195,14 @@ int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t
  *   lse:  device fp32 [B][T][Hq] or NULL;  a row with F_b - T + t < 0 gets
  *         out = 0, lse = -inf.
  *   workspace: device scratch of at least nk_decode_workspace_bytes bytes
- *         holding the split-K partials and one counter per (row, KV head).
- *         It must be zero-filled before its first use; every call leaves the
- *         counters at zero again, so a workspace is zero-filled once and then
- *         reused (two calls that share a workspace must not overlap).
- * Split-K over pages with a log-sum-exp merge done by the last split of each
- * (row, KV head) in the same launch; no host synchronisation, so the call can
- * be captured in a CUDA graph (graph-stable arguments section).  Kernels are
- * launched with programmatic stream serialization (they may start while the
- * previous kernel in the stream drains, and read nothing before it completes).
+ *         holding the split-K partials; no initialisation needed (two calls
+ *         that share a workspace must not overlap).
+ * Split-K over pages, then a log-sum-exp merge kernel launched right behind
+ * (one CTA per row, KV head and 32 dims); no host synchronisation, so the
+ * call can be captured in a CUDA graph (graph-stable arguments section).
+ * Kernels are launched with programmatic stream serialization (they may start
+ * while the previous kernel in the stream drains, and read nothing before it
+ * completes).
  * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T*Hq/H > 64),
  * NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
 int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,
@@ -286,9 +285,8 @@ int nk_pages_from_host(nk_pool* pool, const int32_t* page_ids, int32_t n, const 
  * The first call on a device (with that device current, which must be the
  * pool's device) looks up the array's device address; make it before any
  * stream capture.  All calls share the array, which keeps the last call's
- * contents; each call clears the array's split counters on its stream before
- * the launch.  Two calls that overlap on the GPU race.  Calls no allocating
- * routine. */
+ * contents (every slot a call reads it writes first).  Two calls that overlap
+ * on the GPU race.  Calls no allocating routine. */
 int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* pool,
                                       int32_t layer, const int32_t* block_tables,
                                       const int32_t* table_rows, const int32_t* frontiers,

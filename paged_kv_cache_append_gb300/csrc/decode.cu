@@ -1,10 +1,9 @@
 // decode.cu -- host side of the paged decode attention: split plan,
 // workspace layout and launch.
 //
-// Workspace: [B*H split counters (int, zero between calls)] [per-split (m, l)
-// of every query row] [per-split unnormalised accumulators].  The last CTA of
-// each (row, KV head) merges the splits and resets its counter, so a
-// workspace that starts zero-filled stays valid for every later call.
+// Workspace: [per-split (m, l) of every query row] [per-split unnormalised
+// accumulators].  Every slot the merge reads is written first by the same
+// call, so the workspace needs no initialisation.
 #include <cmath>
 
 #include "decode.cuh"
@@ -13,15 +12,14 @@ namespace nk {
 
 struct DecodePlan {
   int nqt, R, target, ring_bytes;
-  size_t cnt_bytes, ws_ml_bytes, ws_bytes;
+  size_t ws_ml_bytes, ws_bytes;
   DecodeFn fn;
 };
 
 static void plan_sizes(DecodePlan* pl, int B, int H, int D) {
   const size_t parts = static_cast<size_t>(B) * H * pl->target * pl->R;
-  pl->cnt_bytes = (static_cast<size_t>(B) * H * sizeof(int) + 255) / 256 * 256;
   pl->ws_ml_bytes = (parts * sizeof(float2) + 255) / 256 * 256;
-  pl->ws_bytes = pl->cnt_bytes + pl->ws_ml_bytes + parts * D * sizeof(float);
+  pl->ws_bytes = pl->ws_ml_bytes + parts * D * sizeof(float);
 }
 
 static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
@@ -98,9 +96,8 @@ static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t la
   a.vs = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
-  a.counters = static_cast<int*>(workspace);
-  a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + pl.cnt_bytes);
-  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.cnt_bytes + pl.ws_ml_bytes);
+  a.ws_ml = reinterpret_cast<float2*>(workspace);
+  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.ws_ml_bytes);
   a.status = pool->status;
   a.softmax_scale = softmax_scale;
   a.B = B;
@@ -175,7 +172,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   const int H = pool->desc.num_kv_heads, D = pool->desc.head_dim;
   const size_t per_split = static_cast<size_t>(B) * H * pl.R * (sizeof(float2) + D * sizeof(float));
   if (pl.ws_bytes > max_ws) {
-    const size_t fixed = 512 + static_cast<size_t>(B) * H * sizeof(int);
+    const size_t fixed = 512;  // alignment of the (m, l) block
     const size_t fit = max_ws > fixed ? (max_ws - fixed) / per_split : 0;
     if (fit < 1)
       return fail(NK_ERR_WORKSPACE, "one split of this call needs " + std::to_string(per_split + fixed) +
@@ -194,9 +191,8 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.vs = np == 4 ? static_cast<const uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
-  a.counters = static_cast<int*>(scratch);
-  a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(scratch) + pl.cnt_bytes);
-  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(scratch) + pl.cnt_bytes + pl.ws_ml_bytes);
+  a.ws_ml = reinterpret_cast<float2*>(scratch);
+  a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(scratch) + pl.ws_ml_bytes);
   a.status = pool->status;
   a.softmax_scale = softmax_scale;
   a.B = B;
@@ -209,10 +205,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
   a.head_major = pool->desc.order == NK_HEAD_MAJOR;
-  // the scratch is shared by every call: its split counters start at zero
-  cudaError_t e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(B) * H * sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the split counters");
-  e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return NK_OK;
 }

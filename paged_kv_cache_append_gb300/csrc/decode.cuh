@@ -34,8 +34,8 @@
 //       scales folded in as f16 products.
 // At the end the four pairs' (m, l, O) are combined in a fixed order, and the
 // CTA writes unnormalised partials (m, l, acc) to the workspace, or the final
-// out / lse when its row has a single split; the last split of a (row, head)
-// to finish merges them.
+// out / lse when its row has a single split; merge_kernel, launched right
+// behind, combines the splits.
 #pragma once
 
 #include "device.cuh"
@@ -58,7 +58,6 @@ struct DecodeArgs {
   float* lse;
   float2* ws_ml;  // [B][H][maxsplit][R]
   float* ws_acc;  // [B][H][maxsplit][R][D]
-  int* counters;  // [B][H] splits finished; zero between calls (the last CTA resets it)
   int* status;
   // Fused append (nullptr: plain decode): the T new tokens of row b, bf16
   // [B][T][H][D], are encoded into positions F_b - T .. F_b - 1 of the
@@ -198,7 +197,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
   uint64_t* app = empty + NSTAGE;                           // fused append done (NW arrivals)
-  int* s_flags = reinterpret_cast<int*>(app + 1);           // [0] abort, [1] merging CTA
+  int* s_flags = reinterpret_cast<int*>(app + 1);           // [0] abort
   int* s_F = s_flags + 4;                                   // [8] valid length per row
   int* s_row = s_flags + 12;                                // [8] table row per row
   float* s_qmax = reinterpret_cast<float*>(s_flags + 20);   // [8] per-warp max|q|
@@ -868,35 +867,51 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       a.ws_ml[part * R + tid] = make_float2(row_M[tid], row_L[tid]);
     }
   }
-  if (final_out) return;
+}
 
-  // ---- log-sum-exp merge by the last split of this (row, head) to finish ------
-  // Split s holds (m_s, l_s, acc_s); M = max_s m_s, L = sum_s l_s 2^(m_s - M),
-  // out = sum_s acc_s 2^(m_s - M) / L, lse = (M + log2 L) ln 2: the softmax over
-  // the union of the splits' keys.  Partials are published with a device-scope
-  // fence before the counter increment; the last CTA reads them from L2.
-  consumer_sync<NCONS>();
-  if (tid == 0) {
-    // one device-scope fence after the barrier makes every thread's partial
-    // stores visible before the counter increment
-    __threadfence();
-    const int done = atomicAdd(&a.counters[b * a.H + h], 1);
-    s_flags[1] = (done == nsplit - 1);
+// ---- log-sum-exp merge of the splits (separate launch) ----------------------------
+// Split s of (row b, KV head h) holds (m_s, l_s, acc_s) for every query row;
+// M = max_s m_s, L = sum_s l_s 2^(m_s - M), out = sum_s acc_s 2^(m_s - M) / L,
+// lse = (M + log2 L) ln 2: the softmax over the union of the splits' keys.
+// One CTA per (b, h, 32-dim slice), so a row's merge is spread over D / 32
+// SMs; it recomputes the decode's split plan from the same frontiers and
+// returns at once for rows the decode finished in one split.  Launched with
+// programmatic stream serialization right behind the decode: everything
+// before the wait overlaps the decode's tail.
+template <int D, int NQT>
+__global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
+  constexpr int R = 8 * NQT;
+  __shared__ int s_F[8];
+  __shared__ float2 sml[R * kMaxSplits];
+  __shared__ float sw[R * kMaxSplits];
+  __shared__ float4 sacc[4][R * 8];
+  const int b = blockIdx.x, h = blockIdx.y, d0 = blockIdx.z * 32, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < a.B) {
+    const int F = a.frontiers[tid], row = a.table_rows[tid];
+    const bool ok = F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C && (a.k_new == nullptr || F >= a.T);
+    s_F[tid] = ok ? F : 0;
   }
-  consumer_sync<NCONS>();
-  if (!s_flags[1]) return;
-  __threadfence();
-  // (m, l) of every split of every query row, one load each, to shared memory
-  // (the stage ring is free now); then one warp per row: nsplit <= 32 splits,
-  // one per lane
-  float2* sml = reinterpret_cast<float2*>(smem);                  // [R_real][nsplit]
-  float* wgt = reinterpret_cast<float*>(sml + R_real * nsplit);   // [R_real][nsplit]
-  for (int x = tid; x < R_real * nsplit; x += NCONS) {
+  __syncthreads();
+  int total = 0, maxp = 0;
+  for (int bb = 0; bb < a.B; ++bb) {
+    const int np = (s_F[bb] + 63) >> 6;
+    total += np;
+    maxp = max(maxp, np);
+  }
+  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int nsplit = max(1, (((s_F[b] + 63) >> 6) + chunk - 1) / chunk);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (nsplit <= 1) return;  // the decode wrote this row's output
+  const int R_real = a.T * a.G;
+  const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
+  for (int x = tid; x < R_real * nsplit; x += 256) {
     const int qr = x / nsplit, k = x - qr * nsplit;
     sml[x] = __ldcg(&a.ws_ml[(part0 + k) * R + qr]);
   }
-  consumer_sync<NCONS>();
-  for (int qr = warp; qr < R_real; qr += NW) {
+  __syncthreads();
+  for (int qr = warp; qr < R_real; qr += 8) {  // one warp per row, one lane per split
     const float2 ml = lane < nsplit ? sml[qr * nsplit + lane] : make_float2(-INFINITY, 0.f);
     float M = ml.x;
 #pragma unroll
@@ -905,64 +920,54 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     float Ls = ml.y * e;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-    if (lane < nsplit) wgt[qr * nsplit + lane] = Ls > 0.f ? e / Ls : 0.f;
-    if (lane == 0 && a.lse) {
+    if (lane < nsplit) sw[qr * nsplit + lane] = Ls > 0.f ? e / Ls : 0.f;
+    if (lane == 0 && a.lse && blockIdx.z == 0) {
       const int t = qr / a.G, g = qr % a.G;
-      a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] =
-          Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+      a.lse[(static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
   }
-  consumer_sync<NCONS>();
-  // out = sum_s w_s acc_s: four consecutive dims per item (16-byte loads); a
-  // thread takes IPT items and, per round, KB splits of each, so that about
-  // 16 independent loads are in flight per thread
-  {
-    constexpr int NIT = R * (D / 4);                  // items at most (R_real <= R)
-    constexpr int IPT = (NIT + NCONS - 1) / NCONS;
-    constexpr int KB = IPT >= 8 ? 2 : IPT >= 4 ? 4 : IPT >= 2 ? 8 : 16;
-    const int nit = R_real * (D / 4);
-    const int64_t stride = static_cast<int64_t>(R) * D / 4;  // float4 per split
-    const float4* base = reinterpret_cast<const float4*>(a.ws_acc + part0 * R * D);
-    float4 sum[IPT];
+  __syncthreads();
+  // item = (query row, 4 dims of the slice); four threads share an item and
+  // take every fourth split, all of their loads in flight together
+  const int sub = tid & 3;
+  for (int item = tid >> 2; item < R_real * 8; item += 64) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int qr = item >> 3, d = d0 + (item & 7) * 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (part0 * R + qr) * D + d);
+    const int64_t stride = static_cast<int64_t>(R) * D / 4;
+    float4 v[kMaxSplits / 4];
 #pragma unroll
-    for (int it = 0; it < IPT; ++it) sum[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < nsplit; k0 += KB) {
-      float4 v[IPT][KB];
-#pragma unroll
-      for (int it = 0; it < IPT; ++it) {
-        const int x = tid + it * NCONS;
-        const int qr = x / (D / 4), d4 = x % (D / 4);
-#pragma unroll
-        for (int u = 0; u < KB; ++u)
-          v[it][u] = (x < nit && k0 + u < nsplit) ? __ldcg(base + (k0 + u) * stride + qr * (D / 4) + d4)
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int it = 0; it < IPT; ++it) {
-        const int x = tid + it * NCONS;
-        const int qr = x < nit ? x / (D / 4) : 0;
-#pragma unroll
-        for (int u = 0; u < KB; ++u) {
-          const float w = k0 + u < nsplit ? wgt[qr * nsplit + k0 + u] : 0.f;
-          sum[it].x = fmaf(w, v[it][u].x, sum[it].x);
-          sum[it].y = fmaf(w, v[it][u].y, sum[it].y);
-          sum[it].z = fmaf(w, v[it][u].z, sum[it].z);
-          sum[it].w = fmaf(w, v[it][u].w, sum[it].w);
-        }
-      }
+    for (int u = 0; u < kMaxSplits / 4; ++u) {
+      const int k = sub + 4 * u;
+      v[u] = k < nsplit ? __ldcg(src + k * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int it = 0; it < IPT; ++it) {
-      const int x = tid + it * NCONS;
-      if (x >= nit) continue;
-      const int qr = x / (D / 4), d = (x % (D / 4)) * 4;
-      const int t = qr / a.G, g = qr % a.G;
-      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(sum[it].x, sum[it].y), pack_bf16x2(sum[it].z, sum[it].w));
+    for (int u = 0; u < kMaxSplits / 4; ++u) {
+      const int k = sub + 4 * u;
+      const float w = k < nsplit ? sw[qr * nsplit + k] : 0.f;
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
     }
+    sacc[sub][item] = acc;
   }
-  if (tid == 0) a.counters[b * a.H + h] = 0;  // ready for the next call
+  __syncthreads();
+  for (int item = tid; item < R_real * 8; item += 256) {  // the four shares in a fixed order
+    float4 r = sacc[0][item];
+#pragma unroll
+    for (int u = 1; u < 4; ++u) {
+      const float4 x = sacc[u][item];
+      r.x += x.x;
+      r.y += x.y;
+      r.z += x.z;
+      r.w += x.w;
+    }
+    const int qr = item >> 3, d = d0 + (item & 7) * 4;
+    const int t = qr / a.G, g = qr % a.G;
+    __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(r.x, r.y), pack_bf16x2(r.z, r.w));
+  }
 }
 
 template <int KK, int KV, int D, int NQT>
@@ -976,7 +981,9 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, tk, tv, a);
+  cudaError_t e = launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, tk, tv, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(merge_kernel<D, NQT>, dim3(a.B, a.H, D / 32), dim3(256), 0, s, a);
 }
 
 // Bytes of the stage ring, which the final combine and the merge reuse.

@@ -14,11 +14,9 @@
 // where the GPU can reach host memory.  So the first call on a device, with
 // that device current, asks the runtime for the array's device address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture.  All calls share the array and it keeps the last call's contents.
-// Every slot of split partials a call reads it wrote first; the per-(row, KV
-// head) split counters that pick the merging CTA must start at zero, so each
-// call clears them on its stream before the launch (a memset, not an
-// allocation).  Two calls that overlap on the GPU race on the array.
+// capture.  All calls share the array and it keeps the last call's contents;
+// every slot of split partials a call reads it wrote first, so nothing needs
+// clearing.  Two calls that overlap on the GPU race on the array.
 #include <mutex>
 
 #include "internal.h"
