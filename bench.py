@@ -238,8 +238,9 @@ class Bench:
         self.lse = [torch.empty((B, w.T, w.Hq), dtype=torch.float32, device=device) for _ in self.q]
         n = nk.nk_decode_workspace_bytes(self.pool.handle, B, w.T, w.Hq)
         self.ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
-        # one fused append + decode launch per layer (merge in-kernel), or two
-        self.launches_per_step = (1 if fused else 2) * w.num_layers
+        # per layer: the fused append + decode launch and the split merge, or
+        # the append, the decode and the merge
+        self.launches_per_step = (2 if fused else 3) * w.num_layers
         # chunked prefill rows (bf16_prefill): append the chunk, then attend
         self.Bp = len(w.prefill_rows) if share is None else 0
         if self.Bp:
@@ -254,7 +255,8 @@ class Bench:
                 self.cv.append(v.contiguous())
                 self.cout.append(torch.empty_like(self.cq[-1]))
             self.side = torch.cuda.Stream(device=device)
-            self.launches_per_step += 2 * w.num_layers   # chunk append + prefill per layer
+            # chunk append + prefill (+ the dequant pass of quantized pages) per layer
+            self.launches_per_step += (2 if w.profile == "bf16" else 3) * w.num_layers
 
     def _fill(self):
         """Context of every table row (device-side seeded values), written
