@@ -313,7 +313,7 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
  *   pages to fill the last wave of SMs, the split partials and counters.
  * Errors as for decode; NK_ERR_UNSUPPORTED for INT8-G64 pools (their group
  * products are not exact in f16 and per-group accumulators do not fit the
- * tensor memory), for D other than 128 and 256, or a GQA group that does not
+ * tensor memory), for D other than 64, 128 and 256, or a GQA group that does not
  * divide 128 or exceeds 16. */
 int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const nk_pool* pool,
                                int32_t layer, const int32_t* block_tables,

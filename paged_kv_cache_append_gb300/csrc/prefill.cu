@@ -427,7 +427,7 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   if (pool->desc.profile == NK_INT8_G64)
     return fail(NK_ERR_UNSUPPORTED, "chunked prefill is built for BF16, FP8-row, NVFP4-G16 and K8V4 pools");
   const int D = pool->desc.head_dim, H = pool->desc.num_kv_heads;
-  if (D != 128 && D != 256) return fail(NK_ERR_UNSUPPORTED, "chunked prefill needs head_dim 128 or 256");
+  if (D != 64 && D != 128 && D != 256) return fail(NK_ERR_UNSUPPORTED, "chunked prefill needs head_dim 64, 128 or 256");
   if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");
   if (B < 1 || B > pool->desc.max_concurrency) return fail(NK_ERR_SHAPE, "B must be in [1, C]");
   if (Tc < 1) return fail(NK_ERR_SHAPE, "Tc must be >= 1");
@@ -467,8 +467,9 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   if (need && !aligned16(workspace)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
   a.sp = prefill_split_at(workspace, B, H, tiles, nsplit);
   const dim3 grid(tiles * nsplit, H, B);
-  cudaError_t e = D == 256 ? launch_prefill<256>(pool, layer, a, grid, s)
-                           : launch_prefill<128>(pool, layer, a, grid, s);
+  cudaError_t e = D == 256   ? launch_prefill<256>(pool, layer, a, grid, s)
+                  : D == 128 ? launch_prefill<128>(pool, layer, a, grid, s)
+                             : launch_prefill<64>(pool, layer, a, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return NK_OK;
 }

@@ -464,7 +464,9 @@ static cudaError_t launch_passes(const CUtensorMap& tk, const CUtensorMap& tv, c
 
 template <int KK, int KV>
 static cudaError_t launch_qd(int D, const CUtensorMap& tk, const CUtensorMap& tv, const QArgs& a, cudaStream_t s) {
-  return D == 256 ? launch_passes<KK, KV, 256>(tk, tv, a, s) : launch_passes<KK, KV, 128>(tk, tv, a, s);
+  return D == 256   ? launch_passes<KK, KV, 256>(tk, tv, a, s)
+         : D == 128 ? launch_passes<KK, KV, 128>(tk, tv, a, s)
+                    : launch_passes<KK, KV, 64>(tk, tv, a, s);
 }
 
 size_t qprefill_workspace_bytes(const nk_pool* p, int B) {

@@ -72,7 +72,7 @@ def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major"):
             assert torch.all(out[i, Cn:] == 0) and torch.all(torch.isneginf(lse[i, Cn:]))
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("G", [8, 1, 16])
 def test_prefill_small(D, G):
     """Two rows: a mid-page prefix and a ragged chunk that spans several
@@ -105,7 +105,7 @@ def test_prefill_negative_softmax_scale():
 
 
 @pytest.mark.parametrize("profile", ["fp8_row", "nvfp4_g16", "k8v4"])
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("G", [8, 1, 16])
 def test_quantized_prefill_small(profile, D, G):
     """Prefill over FP8-row, NVFP4-G16 and K8V4 pages: a mid-page prefix and a
