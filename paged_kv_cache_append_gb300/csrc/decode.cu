@@ -30,8 +30,10 @@ static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
   const int Rr = T * (Hq / H);
   pl->nqt = Rr <= 8 ? 1 : Rr <= 16 ? 2 : Rr <= 32 ? 4 : 0;
   if (!pl->nqt) return fail(NK_ERR_UNSUPPORTED, "T * Hq / num_kv_heads must be <= 32");
-  if (D == 256 && pl->nqt == 4)
-    return fail(NK_ERR_UNSUPPORTED, "head_dim 256 supports T * Hq / num_kv_heads <= 16");
+  const DecodeFn vfn = vdecode_for(p->desc.profile, D, pl->nqt);
+  if (D == 256 && pl->nqt == 4 && !vfn)
+    return fail(NK_ERR_UNSUPPORTED,
+                "head_dim 256 with T * Hq / num_kv_heads > 16 needs the FP8-row, NVFP4-G16 or K8V4 profile");
   pl->R = 8 * pl->nqt;
   OccFn occ;
   switch (p->desc.profile) {
@@ -41,7 +43,11 @@ static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
     case NK_NVFP4_G16: pl->fn = decode_nvfp4; occ = occupancy_nvfp4; break;
     default: pl->fn = decode_k8v4; occ = occupancy_k8v4; break;
   }
-  const int per_sm = occ(D, pl->nqt, &pl->ring_bytes);
+  int per_sm = occ(D, pl->nqt, &pl->ring_bytes);
+  if (vfn) {  // 17..32 query rows over exact-f16 codes: the tcgen05 kernel, one CTA per SM
+    pl->fn = vfn;
+    per_sm = 1;
+  }
   pl->target = p->num_sms * per_sm / H;
   if (pl->target < 1) pl->target = 1;
   plan_sizes(pl, B, H, D);

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   if constexpr (!Cfg::MMA_BF16) {
     int ex = 0;
     if (mx > 0.f) frexpf(mx, &ex);
-    const int e = mx > 0.f ? 15 - ex : 0;
+    const int e = mx > 0.f ? min(15 - ex, 100) : 0;  // 2^e stays finite in fp32
     qf_mul = ldexpf(1.f, e);
     qscale_log2 = static_cast<float>(e);
   }
@@ -1048,6 +1048,10 @@ cudaError_t decode_int8(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaS
 cudaError_t decode_fp8(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
 cudaError_t decode_nvfp4(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
 cudaError_t decode_k8v4(const nk_pool*, int, const DecodeArgs&, int, dim3, cudaStream_t);
+// The tcgen05 decode (vdecode.cu) for 17..32 query rows per KV head over
+// pages whose codes are exact f16 operands (FP8-row, NVFP4-G16, K8V4); one
+// CTA per SM.  nullptr for other profiles / shapes.
+DecodeFn vdecode_for(int profile, int D, int nqt);
 int occupancy_bf16(int, int, int*);
 int occupancy_int8(int, int, int*);
 int occupancy_fp8(int, int, int*);

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       int ex = 0;
       if (mx > 0.f) frexpf(mx, &ex);
-      const int e = mx > 0.f ? 15 - ex : 0;
+      const int e = mx > 0.f ? min(15 - ex, 100) : 0;  // 2^e stays finite in fp32
       const float qf = ldexpf(1.f, e);
       rs = ldexpf(1.f, -e);
 #pragma unroll 1

@@ -1,0 +1,696 @@
+// vdecode.cu -- decode / verify attention for 17..32 query rows per KV head
+// (T * G > 16, e.g. a 4-token verify with a GQA group of 8) over FP8-row,
+// NVFP4-G16 and K8V4 pools, on the 5th-generation tensor cores.
+//
+// Same contract, split plan, workspace layout and merge as the warp-level
+// decode (decode.cuh): a CTA owns one (row b, KV head h, page range) and
+// writes the final out / lse when its row has one split, else a partial
+// (m, l, acc) that merge_kernel combines.  With 32 query rows the warp-level
+// kernel keeps 128 fp32 accumulators per thread in registers and is bound by
+// its mma.sync issue rate; here S and O live in tensor memory:
+//   S = Q K^T   tcgen05.mma M 128 x N 64 x K D; Q (f16, each query row
+//               scaled by a power of two) in TMEM lanes 0..31, rows 32..127
+//               zero; K = the page tile dequantized to f16 in shared memory;
+//   O += P V    tcgen05.mma M 128 x N D x K 64; P (f16) over its S buffer.
+// Operands are exact: E4M3 and E2M1 codes are f16 values, an E2M1 code times
+// its E4M3 scale is an exact f16 product, FP8-row key scales multiply the fp32
+// scores and FP8-row value scales the softmax weights (with an exact running
+// maximum, so p * s stays finite in f16).
+//
+// Layout of the query rows.  Query row r sits in TMEM lane 32 (r / 8) + r % 8,
+// so that each of the four lane quadrants (and each warp scheduler) holds 8
+// rows; the other 24 lanes of a quadrant carry zero rows of Q.  A softmax warp
+// per quadrant reads S with the 16x256b shape (4 threads per row, 16 keys per
+// thread and page) and writes P back in the same shape, which puts the keys of
+// P in a fixed order inside every 16-key group; the dequantizing warps store
+// the V tile's rows in that order (vrow), so P V sums over matching keys.
+//
+// Warps (448 threads): 0-3 softmax and output (one per quadrant), 4-11
+// dequantize page tiles (and, in the fused call, encode the new tokens first),
+// 12 is the TMA producer of raw code / scale tiles, 13 issues the MMAs.  All
+// waits are bounded.
+#include "decode.cuh"
+#include "tcgen05.cuh"
+
+namespace nk {
+
+template <int KK, int KV, int D>
+struct VCfg {
+  static constexpr int THREADS = 448, NDW = 8;  // threads; dequantizing warps
+  static constexpr int UPT = D / 64;            // 16-code units per dequant thread and tile (4 D units / 256 threads)
+  static constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
+  static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
+  static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
+  static constexpr int R_KS = align_up(64 * KCB, 1024);             // raw stage: K codes, V codes,
+  static constexpr int R_KSC = R_KS + align_up(64 * VCB, 1024);     // K scales, V scales
+  static constexpr int R_VSC = R_KSC + align_up(64 * KSB, 128);
+  static constexpr int RAW = align_up(R_VSC + 64 * VSB, 1024);
+  static constexpr int TX = 64 * (KCB + VCB + KSB + VSB);
+  static constexpr int F16 = 64 * D * 2;
+  static constexpr int NK = 2, NV = D <= 128 ? 3 : 2, NS = 4;
+  // S buffers in TMEM (P is written over its S): three let S run two pages
+  // ahead of P V; at D = 256 the O accumulator leaves room for two
+  static constexpr int NSB = D <= 128 ? 3 : 2, LA = NSB - 1;
+  // raw stages: as many as fit next to the f16 tiles (deeper rings keep more
+  // HBM reads in flight per SM)
+  static constexpr int NR_FIT = (200 * 1024 - (NK + NV) * F16 - 4096) / RAW;
+  static constexpr int NR = NR_FIT < 2 ? 2 : NR_FIT > 8 ? 8 : NR_FIT;
+  static constexpr int OFF_KF = NR * RAW;
+  static constexpr int OFF_VF = OFF_KF + NK * F16;
+  static constexpr int OFF_SC = OFF_VF + NV * F16;   // [NS][128] float: key factors, value scales
+  static constexpr int OFF_BAR = OFF_SC + NS * 128 * 4;
+  static constexpr int NBAR = 2 * NR + 2 * NK + 2 * NV + 2 * NS + 3 * NSB + 3;
+  // at least half of the SM's shared memory: one CTA per SM owns all 512 TMEM columns
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 128 + 1024;
+  static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
+  static constexpr uint32_t COL_S = 0, COL_Q = 64 * NSB, COL_O = 256;
+  static_assert(COL_Q + D / 2 <= COL_O && COL_O + D <= 512, "TMEM columns");
+  static constexpr uint32_t ID_S = tc::idesc_f16(128, 64, false, false);
+  static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
+  static constexpr float THR = KV == KIND_FP8 ? 0.f : 8.f;  // exact maximum when P carries V scales
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static_assert(UPT * 32 * NDW == 4 * D, "units per tile");
+};
+
+// Four E4M3 codes -> two f16x2 (exact).
+__device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Eight E2M1 codes (low nibble first) -> four f16x2 (exact).
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2, uint32_t& h3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+
+// Row of the V tile that holds key r of the page: inside each 16-key group,
+// key bits (b3 b2 b1 b0) go to row bits (b2 b1 b3 b0), the order in which the
+// softmax warps' 16x256b stores lay out P.
+__device__ __forceinline__ int vrow(int r) { return (r & ~15) | ((r & 6) << 1) | ((r & 8) >> 2) | (r & 1); }
+
+// Shared-memory offsets of unit u of a page tile: 16 consecutive dims
+// [16 q, 16 q + 16) of key r (u = r * D / 16 + q), in the raw code / scale
+// tile and in the 128-byte-swizzled K-major f16 tile the MMA reads (64-dim
+// halves of 64 rows x 128 bytes).
+struct DqOff {
+  int src, sc, dst0, dst1, key;
+};
+
+template <int KIND, int D, bool PERM>
+__device__ __forceinline__ DqOff dq_offsets(int u) {
+  constexpr int CB = code_row_bytes<KIND>(D), RB = CB < 128 ? CB : 128, SB = scale_row_bytes<KIND>(D);
+  const int r = u / (D / 16), q = u % (D / 16);
+  const int col = KIND == KIND_FP8 ? 16 * q : 8 * q;
+  const int row = PERM ? vrow(r) : r;
+  DqOff o;
+  o.src = (col / RB) * (64 * RB) + static_cast<int>(swz<RB>(r, col % RB));
+  o.sc = r * SB + q;
+  o.dst0 = (q / 4) * 8192 + static_cast<int>(swz<128>(row, (q % 4) * 32));
+  o.dst1 = (q / 4) * 8192 + static_cast<int>(swz<128>(row, (q % 4) * 32 + 16));
+  o.key = r;
+  return o;
+}
+
+// One unit: 16 codes to 16 exact f16 values (zero when the key lies past the
+// frontier).
+template <int KIND>
+__device__ __forceinline__ void deq(const uint8_t* codes, const uint8_t* scales, uint8_t* tile, const DqOff& o,
+                                    bool zero) {
+  uint32_t h[8];
+  if (zero) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = 0u;
+  } else if constexpr (KIND == KIND_FP8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(codes + o.src);
+    e4m3x4_f16(w.x, h[0], h[1]);
+    e4m3x4_f16(w.y, h[2], h[3]);
+    e4m3x4_f16(w.z, h[4], h[5]);
+    e4m3x4_f16(w.w, h[6], h[7]);
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2*>(codes + o.src);
+    const uint32_t sbyte = scales[o.sc];
+    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(sbyte * 0x101u));  // the scale in both halves
+    e2m1x8_f16(w.x, h[0], h[1], h[2], h[3]);
+    e2m1x8_f16(w.y, h[4], h[5], h[6], h[7]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = hmul2_u32(h[i], s2);
+  }
+  *reinterpret_cast<uint4*>(tile + o.dst0) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(tile + o.dst1) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// True in one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+__device__ __forceinline__ void v_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int KK, int KV, int D>
+__global__ void __launch_bounds__(448, 1)
+    vdecode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, DecodeArgs a) {
+  using Cfg = VCfg<KK, KV, D>;
+  constexpr int NR = Cfg::NR, NK = Cfg::NK, NV = Cfg::NV, NS = Cfg::NS, NDW = Cfg::NDW;
+  constexpr int NSB = Cfg::NSB, LA = Cfg::LA;
+  constexpr int R = 32;  // query rows of a part in the workspace
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sKf = smem + Cfg::OFF_KF;
+  uint8_t* sVf = smem + Cfg::OFF_VF;
+  float* sSc = reinterpret_cast<float*>(smem + Cfg::OFF_SC);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + NR;
+  uint64_t* kf_full = raw_empty + NR;
+  uint64_t* kf_empty = kf_full + NK;
+  uint64_t* vf_full = kf_empty + NK;
+  uint64_t* vf_empty = vf_full + NV;
+  uint64_t* sc_full = vf_empty + NV;
+  uint64_t* sc_empty = sc_full + NS;
+  uint64_t* s_full = sc_empty + NS;     // [NSB]: S(j) in buffer j % NSB
+  uint64_t* p_full = s_full + NSB;      // [NSB]: P(j) written over it
+  uint64_t* o_done = p_full + NSB;      // [NSB]: P V(j) accumulated
+  uint64_t* q_ready = o_done + NSB;
+  uint64_t* app = q_ready + 1;
+  uint64_t* drain = app + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  int* s_F = reinterpret_cast<int*>(tslot + 2);     // [8]
+  int* s_row = s_F + 8;                             // [8]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y;
+  if (tid == 0) {
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], NDW);
+    }
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&kf_full[i], NDW);
+      mbar_init(&kf_empty[i], 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&vf_full[i], NDW);
+      mbar_init(&vf_empty[i], 1);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sc_full[i], NDW);
+      mbar_init(&sc_empty[i], 4);
+    }
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(q_ready, 4);  // the four softmax warps (query rows and zero rows of Q)
+    mbar_init(app, NDW);
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  // The fused call reads tables, row map, frontiers and earlier pages before
+  // the programmatic dependency wait (see decode.cuh); q, k, v and every
+  // global write come after it.
+  const bool early = a.k_new != nullptr;
+  if (!early) griddep_wait();
+  griddep_launch_dependents();
+  if (tid < a.B) {
+    const int F = a.frontiers[tid], row = a.table_rows[tid];
+    const bool ok = F >= 0 && F <= a.L * 64 && row >= 0 && row < a.C && (a.k_new == nullptr || F >= a.T);
+    if (!ok && blockIdx.x == 0 && h == 0) set_status(a.status, NK_STATUS_FRONTIER);
+    s_F[tid] = ok ? F : 0;
+    s_row[tid] = ok ? row : 0;
+  }
+  if (warp == 0) {
+    tc::alloc(tslot, 512);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+
+  // ---- the split plan of decode.cuh --------------------------------------------
+  int total = 0, maxp = 0;
+  for (int bb = 0; bb < a.B; ++bb) {
+    const int np = (s_F[bb] + 63) >> 6;
+    total += np;
+    maxp = max(maxp, np);
+  }
+  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  int b = -1, split = 0, nsplit = 0, npages = 0;
+  {
+    int acc = 0;
+    for (int bb = 0; bb < a.B; ++bb) {
+      const int np = (s_F[bb] + 63) >> 6;
+      const int ns = max(1, (np + chunk - 1) / chunk);
+      if (static_cast<int>(blockIdx.x) < acc + ns) {
+        b = bb;
+        split = blockIdx.x - acc;
+        nsplit = ns;
+        npages = np;
+        break;
+      }
+      acc += ns;
+    }
+  }
+  const int F = b >= 0 ? s_F[b] : 0;
+  const int p0 = split * chunk;
+  const int n = b >= 0 ? min(chunk, npages - p0) : 0;
+  const int app_lo = early ? (F - a.T) >> 6 : 0x7fffffff;
+  const int R_real = a.T * a.G;
+  const int32_t* trow = a.tables + static_cast<int64_t>(b >= 0 ? s_row[b] : 0) * a.L;
+
+  if (b < 0) {
+    // no work: only the TMEM allocation is released below
+  } else if (warp == 12) {
+    // -------------------- TMA producer of raw code / scale tiles --------------------
+    if (lane == 0) {
+      bool app_seen = false;
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        int g = trow[p0 + i];
+        if (g < 0 || g >= a.M) {
+          set_status(a.status, NK_STATUS_PAGE_RANGE);
+          g = 0;
+        }
+        const int s = i % NR;
+        if (p0 + i >= app_lo && !app_seen) {  // this page receives new tokens: wait for them
+          app_seen = true;
+          if (!mbar_wait_bounded(app, 0, a.status)) { *s_abort = 1; break; }
+        }
+        if (i >= NR && !mbar_wait_bounded(&raw_empty[s], ((i / NR) - 1) & 1, a.status)) { *s_abort = 1; break; }
+        uint8_t* st = smem + s * Cfg::RAW;
+        const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
+        mbar_arrive_expect_tx(&raw_full[s], Cfg::TX);
+#pragma unroll
+        for (int c = 0; c < Cfg::KCB / Cfg::K_RB; ++c)
+          tma_load_2d(st + c * 64 * Cfg::K_RB, &tmk, c * Cfg::K_RB, y, &raw_full[s]);
+#pragma unroll
+        for (int c = 0; c < Cfg::VCB / Cfg::V_RB; ++c)
+          tma_load_2d(st + Cfg::R_KS + c * 64 * Cfg::V_RB, &tmv, c * Cfg::V_RB, y, &raw_full[s]);
+        bulk_load(st + Cfg::R_KSC, a.ks + static_cast<int64_t>(y) * Cfg::KSB, 64 * Cfg::KSB, &raw_full[s]);
+        bulk_load(st + Cfg::R_VSC, a.vs + static_cast<int64_t>(y) * Cfg::VSB, 64 * Cfg::VSB, &raw_full[s]);
+        ++issued;
+      }
+      // after an abort, the copies still in flight land before the CTA exits
+      for (int i = issued > NR ? issued - NR : 0; i < issued; ++i)
+        mbar_wait_bounded(&raw_full[i % NR], (i / NR) & 1, a.status, 100000000ull);
+    }
+  } else if (warp == 13) {
+    // ------------------------------ MMA issuer --------------------------------
+    // The whole warp runs the loop, so the operand descriptors are warp-uniform
+    // values; one elected lane issues the MMAs and commits.
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(q_ready, 0, a.status));
+    tc::fence_after();
+    const uint32_t k_base = smem_u32(sKf), v_base = smem_u32(sVf);
+    // issue order S(0) .. S(LA - 1), then S(j), P V(j - LA) for every j
+    for (int j = 0; ok && j < n + LA; ++j) {
+      if (j < n) {
+        const int ks = j % NK, sb = j % NSB;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&kf_full[ks], (j / NK) & 1, a.status) && !*s_abort);
+        if (!ok) break;
+        tc::fence_after();
+        const uint64_t kd = tc::smem_desc(k_base + ks * Cfg::F16, 16, 1024);
+        const uint32_t sd = tmem + Cfg::COL_S + 64 * sb;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma_ts(sd, tmem + Cfg::COL_Q + kk * 8,
+                       kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
+          tc::commit(&s_full[sb]);
+          tc::commit(&kf_empty[ks]);
+        }
+        __syncwarp();
+      }
+      if (j >= LA) {
+        const int jj = j - LA, vs = jj % NV, pb = jj % NSB;
+        ok = mbar_wait_bounded(&vf_full[vs], (jj / NV) & 1, a.status) && !*s_abort;
+        if (ok) ok = mbar_wait_bounded(&p_full[pb], (jj / NSB) & 1, a.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc::fence_after();
+        const uint64_t vd = tc::smem_desc(v_base + vs * Cfg::F16, 8192, 1024);
+        const uint32_t pa = tmem + Cfg::COL_S + 64 * pb;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_ts(tmem + Cfg::COL_O, pa + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), Cfg::ID_O,
+                       (jj > 0 || kk > 0));
+          tc::commit(&o_done[pb]);
+          tc::commit(&vf_empty[vs]);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      if (!ok) *s_abort = 1;
+      tc::commit(drain);
+    }
+  } else if (warp >= 4) {
+    // ----------------- dequantize warps (and the fused append) ------------------
+    const int dw = warp - 4;          // 0..7
+    const int dt = dw * 32 + lane;    // 0..255
+    DqOff ko[Cfg::UPT], vo[Cfg::UPT];
+#pragma unroll
+    for (int k = 0; k < Cfg::UPT; ++k) {
+      ko[k] = dq_offsets<KK, D, false>(dt + 256 * k);
+      vo[k] = dq_offsets<KV, D, true>(dt + 256 * k);
+    }
+    if (early) griddep_wait();
+    if (early) {  // the new tokens whose pages this CTA reads, one warp per token
+      constexpr int KCBW = code_row_bytes<KK>(D), VCBW = code_row_bytes<KV>(D);
+      constexpr int KSBW = scale_row_bytes<KK>(D), VSBW = scale_row_bytes<KV>(D);
+      for (int t = dw; t < a.T; t += NDW) {
+        const int pos = F - a.T + t, pg = pos >> 6;
+        if (pg < p0 || pg >= p0 + n) continue;
+        const int g = trow[pg];
+        if (g < 0 || g >= a.M) {
+          if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
+          continue;
+        }
+        const int64_t token_row = tile_row(g, h, a.H, a.M, a.head_major) + (pos & 63);
+        const int64_t src = ((static_cast<int64_t>(b) * a.T + t) * a.H + h) * D;
+        encode_row<KK, D>(a.k_new + src, a.kc_w + token_row * KCBW, a.ks_w + token_row * KSBW, lane);
+        encode_row<KV, D>(a.v_new + src, a.vc_w + token_row * VCBW, a.vs_w + token_row * VSBW, lane);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) v_arrive(app);
+    }
+    for (int i = 0; i < n; ++i) {
+      const int s = i % NR;
+      bool ok = mbar_wait_bounded(&raw_full[s], (i / NR) & 1, a.status) && !*s_abort;
+      const uint8_t* st = smem + s * Cfg::RAW;
+      const int kvalid = F - 64 * (p0 + i);  // V rows >= kvalid lie past the frontier
+      if (ok && i >= NK) ok = mbar_wait_bounded(&kf_empty[i % NK], ((i / NK) - 1) & 1, a.status);
+      if (ok) {
+        uint8_t* kt = sKf + (i % NK) * Cfg::F16;
+#pragma unroll
+        for (int k = 0; k < Cfg::UPT; ++k) deq<KK>(st, st + Cfg::R_KSC, kt, ko[k], false);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) v_arrive(&kf_full[i % NK]);
+      if (ok && i >= NV) ok = mbar_wait_bounded(&vf_empty[i % NV], ((i / NV) - 1) & 1, a.status);
+      if (ok) {
+        uint8_t* vt = sVf + (i % NV) * Cfg::F16;
+#pragma unroll
+        for (int k = 0; k < Cfg::UPT; ++k) deq<KV>(st + Cfg::R_KS, st + Cfg::R_VSC, vt, vo[k], vo[k].key >= kvalid);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) v_arrive(&vf_full[i % NV]);
+      if (ok && i >= NS) ok = mbar_wait_bounded(&sc_empty[i % NS], ((i / NS) - 1) & 1, a.status);
+      if (ok && dt < 64) {
+        float* sc = sSc + (i % NS) * 128;
+        float kscale = 1.f, vscale = 1.f;
+        if constexpr (KK == KIND_FP8) kscale = __half2float(*reinterpret_cast<const __half*>(st + Cfg::R_KSC + dt * 2));
+        if constexpr (KV == KIND_FP8) vscale = __half2float(*reinterpret_cast<const __half*>(st + Cfg::R_VSC + dt * 2));
+        sc[dt] = kscale * a.softmax_scale * kLog2e;
+        sc[64 + dt] = dt < kvalid ? vscale : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        v_arrive(&sc_full[i % NS]);
+        v_arrive(&raw_empty[s]);
+      }
+      if (!ok) {
+        *s_abort = 1;
+        break;
+      }
+    }
+  } else {
+    // ---------- softmax and output: warp w owns query rows [8 w, 8 w + 8) ----------
+    const int s4 = lane & 3, rl = lane >> 2;  // this thread: row rl of the quadrant, keys 8k + 2 s4 + {0, 1}
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const int qr = 8 * warp + rl;
+    const bool row_real = qr < R_real;
+    const int lim = F - a.T + qr / a.G;  // keys <= lim are visible to this query row
+    if (early) griddep_wait();
+    float rs_q = 1.f;  // 2^-e of query row 8 w + lane (lanes 0..7)
+    {
+      const int myq = 8 * warp + lane;
+      const bool q_real = lane < 8 && myq < R_real;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((static_cast<int64_t>(b) * a.T + myq / a.G) * a.Hq + h * a.G + myq % a.G) * D);
+      float mx = 0.f;
+      if (q_real)
+        for (int u = 0; u < D / 8; ++u) {
+          const uint4 x = src[u];
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(__bfloat162float(e[k])));
+        }
+      int ex = 0;
+      if (mx > 0.f) frexpf(mx, &ex);
+      const int e = mx > 0.f ? min(15 - ex, 100) : 0;  // 2^e stays finite in fp32
+      const float qf = ldexpf(1.f, e);
+      rs_q = ldexpf(1.f, -e);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {  // lanes 8..31 write zero rows
+        uint32_t qv[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = q_real ? src[c0 / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+            qv[4 * u + k] = pack_f16x2(__low2float(v) * qf, __high2float(v) * qf);
+          }
+        }
+        tc::st32(tmem + lb + Cfg::COL_Q + c0, qv);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) v_arrive(q_ready);
+    }
+    const float rs = __shfl_sync(0xffffffffu, rs_q, rl);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int sb = j % NSB, ss = j % NS;
+      ok = mbar_wait_bounded(&s_full[sb], (j / NSB) & 1, a.status) && !*s_abort;
+      if (ok) ok = mbar_wait_bounded(&sc_full[ss], (j / NS) & 1, a.status) && !*s_abort;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        *s_abort = 1;
+        break;
+      }
+      tc::fence_after();
+      float x[16];
+      {
+        uint32_t v[32];
+        tc::ld16x256_x8(tmem + lb + Cfg::COL_S + 64 * sb, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          x[2 * k] = __uint_as_float(v[4 * k]);
+          x[2 * k + 1] = __uint_as_float(v[4 * k + 1]);
+        }
+      }
+      const float* ksc = sSc + ss * 128 + 2 * s4;  // + 8 k: factors of keys 8k + 2 s4 + {0, 1}
+      const int key0 = 64 * (p0 + j) + 2 * s4;
+      if (64 * (p0 + j) + 63 <= F - a.T) {  // every key of the page is visible to every row
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 kf = *reinterpret_cast<const float2*>(ksc + 8 * k);
+          x[2 * k] = row_real ? x[2 * k] * kf.x : -INFINITY;
+          x[2 * k + 1] = row_real ? x[2 * k + 1] * kf.y : -INFINITY;
+        }
+      } else {
+        const int kmax = row_real ? lim - key0 : -1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 kf = *reinterpret_cast<const float2*>(ksc + 8 * k);
+          x[2 * k] = 8 * k <= kmax ? x[2 * k] * kf.x : -INFINITY;
+          x[2 * k + 1] = 8 * k + 1 <= kmax ? x[2 * k + 1] * kf.y : -INFINITY;
+        }
+      }
+      // row maximum: a tree over this thread's 16 keys, then over the row's 4 threads
+      float mt[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mt[u] = fmaxf(fmaxf(x[u], x[u + 4]), fmaxf(x[u + 8], x[u + 12]));
+      float pm = fmaxf(fmaxf(mt[0], mt[1]), fmaxf(mt[2], mt[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+      const float rmax = pm == -INFINITY ? -INFINITY : pm * rs;
+      float factor = 1.f;
+      const float mnew = fmaxf(m_used, rmax);
+      bool resc = false;
+      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + Cfg::THR)) {
+        factor = m_used == -INFINITY ? 0.f : ex2(m_used - mnew);
+        m_used = mnew;
+        resc = true;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      uint32_t pk[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float p0v = ex2(fmaf(x[2 * k], rs, -mu));
+        float p1v = ex2(fmaf(x[2 * k + 1], rs, -mu));
+        ps[k & 3] += p0v + p1v;
+        if constexpr (KV == KIND_FP8) {
+          const float2 vf = *reinterpret_cast<const float2*>(ksc + 64 + 8 * k);
+          p0v *= vf.x;
+          p1v *= vf.y;
+        }
+        // S repetition k -> P columns 8 (k / 2) + 2 s4 + (k % 2) of lane rl
+        pk[4 * (k >> 1) + (k & 1)] = pack_f16x2(p0v, p1v);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {  // lanes 8..15 of the quadrant: zero rows
+        pk[4 * jj + 2] = 0u;
+        pk[4 * jj + 3] = 0u;
+      }
+      l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      __syncwarp();
+      if (lane == 0) v_arrive(&sc_empty[ss]);
+      // O is rescaled only when a row's maximum moved: then P V(j - 1) must
+      // have landed first (P V(j - 1 - NSB) has, as S(j) has completed, so
+      // the parity of o_done[(j - 1) % NSB] is unambiguous); P V(j) waits
+      // for this warp's P either way
+      if (__any_sync(0xffffffffu, resc && j >= 1)) {
+        const int jp = j - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&o_done[jp % NSB], (jp / NSB) & 1, a.status) && !*s_abort);
+        if (!ok) {
+          *s_abort = 1;
+          break;
+        }
+        tc::fence_after();
+        const float f = (resc && j >= 1) ? factor : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t ov[32];
+          tc::ld16x256_x8(tmem + lb + Cfg::COL_O + c0, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * f);
+            ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * f);
+          }
+          tc::st16x256_x8(tmem + lb + Cfg::COL_O + c0, ov);
+        }
+      }
+      tc::st16x256_x4(tmem + lb + Cfg::COL_S + 64 * sb, pk);
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) v_arrive(&p_full[sb]);
+    }
+    // every MMA of the CTA has completed once drain has (committed after the last P V)
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(drain, 0, a.status) && !*s_abort);
+    tc::fence_after();
+    // row sums over the row's 4 threads (fixed order), then lane L < 8 writes row 8 w + L
+    float lr = l + __shfl_xor_sync(0xffffffffu, l, 1);
+    lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+    const float lt = __shfl_sync(0xffffffffu, lr, 4 * (lane & 7));
+    const float mt_row = __shfl_sync(0xffffffffu, m_used, 4 * (lane & 7));
+    const int orow = 8 * warp + lane;
+    const bool out_real = lane < 8 && orow < R_real;
+    const int ot = orow / a.G, og = orow % a.G;
+    if (ok) {
+      // the split's result: final out / lse (one split) or the partial (m, l, acc)
+      const bool final_out = nsplit == 1;
+      const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + split;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (n > 0) {
+          tc::ld32(tmem + lb + Cfg::COL_O + c0, ov);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (!out_real) continue;
+        if (final_out) {
+          __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og) * D + c0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(
+                pack_bf16x2(__uint_as_float(ov[8 * c]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
+        } else {
+          float* dst = a.ws_acc + (part * R + orow) * D + c0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst + 4 * c) = make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+        }
+      }
+      if (out_real) {
+        if (final_out) {
+          if (a.lse)
+            a.lse[(static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og] =
+                lt > 0.f ? (mt_row + log2f(lt)) * kLn2 : -INFINITY;
+        } else {
+          a.ws_ml[part * R + orow] = make_float2(n > 0 ? mt_row : -INFINITY, n > 0 ? lt : 0.f);
+        }
+      }
+    }
+  }
+
+  if (warp == 0 && lane == 0 && b >= 0) mbar_wait_bounded(drain, 0, a.status, 200000000ull);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+template <int KK, int KV, int D>
+static cudaError_t launch_v(const nk_pool* p, int layer, const DecodeArgs& a, dim3 grid, cudaStream_t s) {
+  using Cfg = VCfg<KK, KV, D>;
+  auto k = vdecode_kernel<KK, KV, D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaError_t e = launch_pdl(k, grid, dim3(Cfg::THREADS), Cfg::SMEM, s, p->tmap[layer * 2 + 0], p->tmap[layer * 2 + 1], a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(merge_kernel<D, 4>, dim3(a.B, a.H, D / 32), dim3(256), 0, s, a);
+}
+
+template <int KK, int KV>
+static cudaError_t vdispatch(const nk_pool* p, int layer, const DecodeArgs& a, int nqt, dim3 grid, cudaStream_t s) {
+  if (nqt != 4) return cudaErrorInvalidValue;
+  switch (p->desc.head_dim) {
+    case 64: return launch_v<KK, KV, 64>(p, layer, a, grid, s);
+    case 128: return launch_v<KK, KV, 128>(p, layer, a, grid, s);
+    case 256: return launch_v<KK, KV, 256>(p, layer, a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+DecodeFn vdecode_for(int profile, int D, int nqt) {
+  if (nqt != 4 || (D != 64 && D != 128 && D != 256)) return nullptr;
+  switch (profile) {
+    case NK_FP8_E4M3_ROW: return vdispatch<KIND_FP8, KIND_FP8>;
+    case NK_NVFP4_G16: return vdispatch<KIND_NVFP4, KIND_NVFP4>;
+    case NK_K8V4: return vdispatch<KIND_FP8, KIND_NVFP4>;
+    default: return nullptr;
+  }
+}
+
+}  // namespace nk

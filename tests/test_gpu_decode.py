@@ -299,3 +299,70 @@ def test_head_major_shared_prefix_with_cow_tail():
     assert not sc.planes_equal(0)
     ref_out, ref_lse = sc.oracle_decode(0, q, fr)
     compare_attention(out, lse, ref_out, ref_lse)
+
+
+# ---- 17..32 query rows per KV head over FP8-row / NVFP4-G16 / K8V4 pages --------
+# These shapes run the tcgen05 decode kernel (Q and the accumulators in tensor
+# memory); the same split plan and merge as the warp-level kernel.
+
+@pytest.mark.parametrize("profile", ["fp8_row", "nvfp4_g16", "k8v4"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G,T", [(8, 4), (6, 3), (32, 1), (16, 2)])
+@pytest.mark.parametrize("fused", [False, True], ids=["append_then_decode", "fused"])
+def test_wide_query_groups(profile, D, G, T, fused):
+    """T * G in 17..32 (18 leaves a ragged last 8-row group): a row with a
+    frontier inside its first page, one just past a page edge, and one long
+    enough to be split."""
+    Hkv = 1 if G >= 16 else 2
+    w = small(profile, Hkv, G, D, 3000, 3, T, seed=D * 7 + G * 3 + T + (1 if fused else 0),
+              contexts=[0, 62, 3000 - T])
+    run_and_check(w, fused=fused)
+
+
+@pytest.mark.parametrize("profile", ["fp8_row", "nvfp4_g16", "k8v4"])
+def test_wide_query_groups_stale_tail_and_negative_scale(profile):
+    """Bytes past each frontier poisoned with 0xFF on the GPU (NaN codes and
+    scales), and a negative softmax scale, at T * G = 32."""
+    import dataclasses
+    w = small(profile, 2, 8, 128, 1024, 4, 4, seed=61, contexts=[10, 200, 333, 700])
+    w = dataclasses.replace(w, scale=-w.scale)
+    sc = Scenario(w)
+    k, v = w.step_kv(0)
+    dev = "cuda"
+    tr = torch.from_numpy(w.table_rows).to(dev)
+    fr = torch.from_numpy(w.context + 4).to(dev)
+    sc.gpu.append(0, sc.tables_d, tr, torch.from_numpy(w.context).to(dev), k.to(dev), v.to(dev))
+    from paged_kv_cache_append_gb300.workloads import bf16_to_bits
+    sc.orc.append(0, w.tables, w.table_rows, w.context, bf16_to_bits(k), bf16_to_bits(v))
+    for b in range(w.B):
+        F = int(w.context[b]) + 4
+        g = int(w.tables[b, F // 64])
+        for i, plane in enumerate(sc.gpu.planes[0]):
+            rb = sc.gpu.row_bytes[i]
+            for h in range(w.Hkv):
+                base = ((g * w.Hkv + h) * 64) * rb
+                plane[base + (F % 64) * rb: base + 64 * rb] = 0xFF
+    q = w.step_q(0)
+    out, lse = sc.gpu.decode(0, q.to(dev), sc.tables_d, tr, fr, w.scale)
+    ref_out, ref_lse = sc.oracle_decode(0, q, w.context + 4)
+    compare_attention(out.cpu(), lse.cpu(), ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("profile", ["fp8_row", "k8v4"])
+@pytest.mark.parametrize("fused", [False, True], ids=["append_then_decode", "fused"])
+def test_wide_query_groups_head_major(profile, fused):
+    w = small(profile, 2, 8, 256, 700, 3, 4, seed=307, contexts=[0, 190, 696])
+    run_and_check(w, fused=fused, order="head_major")
+
+
+def test_wide_query_groups_at_head_dim_256_need_exact_f16_codes():
+    """T * G > 16 at head_dim 256 is served by the tcgen05 kernel only; the
+    BF16 and INT8-G64 profiles reject it before launching anything."""
+    for profile in ("bf16", "int8_g64"):
+        w = small(profile, 2, 8, 256, 300, 2, 4, seed=5, contexts=[10, 20])
+        sc = Scenario(w, oracle=False)
+        dev = "cuda"
+        with pytest.raises(nk.NkError) as e:
+            sc.gpu.decode(0, w.step_q(0).to(dev), sc.tables_d, torch.from_numpy(w.table_rows).to(dev),
+                          torch.from_numpy(w.context + 4).to(dev), w.scale)
+        assert e.value.code == -4   # NK_ERR_UNSUPPORTED
