@@ -7,11 +7,12 @@
 // writes the final out / lse when its row has one split, else a partial
 // (m, l, acc) that merge_kernel combines.  With 32 query rows the warp-level
 // kernel keeps 128 fp32 accumulators per thread in registers and is bound by
-// its mma.sync issue rate; here S and O live in tensor memory:
-//   S = Q K^T   tcgen05.mma M 128 x N 64 x K D; Q (f16, each query row
-//               scaled by a power of two) in TMEM lanes 0..31, rows 32..127
-//               zero; K = the page tile dequantized to f16 in shared memory;
-//   O += P V    tcgen05.mma M 128 x N D x K 64; P (f16) over its S buffer.
+// its mma.sync issue rate; here S and O live in tensor memory.  A key tile is
+// TK = 128 keys (two pages) at head_dim <= 128, one page at 256:
+//   S = Q K^T   tcgen05.mma M 128 x N TK x K D; Q (f16, each query row scaled
+//               by a power of two) in TMEM, K = the tile dequantized to f16 in
+//               shared memory;
+//   O += P V    tcgen05.mma M 128 x N D x K TK; P (f16) over its S buffer.
 // Operands are exact: E4M3 and E2M1 codes are f16 values, an E2M1 code times
 // its E4M3 scale is an exact f16 product, FP8-row key scales multiply the fp32
 // scores and FP8-row value scales the softmax weights (with an exact running
@@ -20,14 +21,14 @@
 // Layout of the query rows.  Query row r sits in TMEM lane 32 (r / 8) + r % 8,
 // so that each of the four lane quadrants (and each warp scheduler) holds 8
 // rows; the other 24 lanes of a quadrant carry zero rows of Q.  A softmax warp
-// per quadrant reads S with the 16x256b shape (4 threads per row, 16 keys per
-// thread and page) and writes P back in the same shape, which puts the keys of
-// P in a fixed order inside every 16-key group; the dequantizing warps store
-// the V tile's rows in that order (vrow), so P V sums over matching keys.
+// per quadrant reads S with the 16x256b shape (4 threads per row) and writes P
+// back in the same shape, which puts the keys of P in a fixed order inside
+// every 16-key group; the dequantizing warps store the V tile's rows in that
+// order (vrow), so P V sums over matching keys.
 //
 // Warps (448 threads): 0-3 softmax and output (one per quadrant), 4-11
-// dequantize page tiles (and, in the fused call, encode the new tokens first),
-// 12 is the TMA producer of raw code / scale tiles, 13 issues the MMAs.  All
+// dequantize key tiles (and, in the fused call, encode the new tokens first),
+// 12 is the TMA producer of raw code / scale pages, 13 issues the MMAs.  All
 // waits are bounded.
 #include "decode.cuh"
 #include "tcgen05.cuh"
@@ -37,39 +38,43 @@ namespace nk {
 template <int KK, int KV, int D>
 struct VCfg {
   static constexpr int THREADS = 448, NDW = 8;  // threads; dequantizing warps
-  static constexpr int UPT = D / 64;            // 16-code units per dequant thread and tile (4 D units / 256 threads)
+  static constexpr int TK = D <= 128 ? 128 : 64, PPT = TK / 64;  // keys and pages of a tile
+  // 8-code units: thread dt of the dequantizing warps converts column unit
+  // p = dt % (D / 8) of rows r0 + RPT k, r0 = dt / (D / 8), of every page
+  static constexpr int RPT = 2048 / D, PASSES = 64 / RPT;
   static constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
   static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
   static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
-  static constexpr int R_KS = align_up(64 * KCB, 1024);             // raw stage: K codes, V codes,
+  static constexpr int R_KS = align_up(64 * KCB, 1024);             // raw page stage: K codes, V codes,
   static constexpr int R_KSC = R_KS + align_up(64 * VCB, 1024);     // K scales, V scales
   static constexpr int R_VSC = R_KSC + align_up(64 * KSB, 128);
   static constexpr int RAW = align_up(R_VSC + 64 * VSB, 1024);
   static constexpr int TX = 64 * (KCB + VCB + KSB + VSB);
-  static constexpr int F16 = 64 * D * 2;
-  static constexpr int NK = 2, NV = D <= 128 ? 3 : 2, NS = 4;
-  // S buffers in TMEM (P is written over its S): three let S run two pages
-  // ahead of P V; at D = 256 the O accumulator leaves room for two
-  static constexpr int NSB = D <= 128 ? 3 : 2, LA = NSB - 1;
-  // raw stages: as many as fit next to the f16 tiles (deeper rings keep more
-  // HBM reads in flight per SM)
-  static constexpr int NR_FIT = (200 * 1024 - (NK + NV) * F16 - 4096) / RAW;
-  static constexpr int NR = NR_FIT < 2 ? 2 : NR_FIT > 8 ? 8 : NR_FIT;
+  static constexpr int F16 = TK * D * 2;       // f16 tile: D / 64 chunks of TK rows x 128 bytes
+  static constexpr int CHUNK = TK * 128;
+  static constexpr int NK = 2, NV = 2, NS = 4;
+  static constexpr int NSB = 2;                // S buffers in TMEM (P is written over its S)
+  // raw page stages: as many as fit next to the f16 tiles
+  static constexpr int NR_FIT = (204 * 1024 - (NK + NV) * F16 - 6144) / RAW;
+  static constexpr int NR = NR_FIT < 2 * PPT ? 2 * PPT : NR_FIT > 8 ? 8 : NR_FIT;
   static constexpr int OFF_KF = NR * RAW;
   static constexpr int OFF_VF = OFF_KF + NK * F16;
-  static constexpr int OFF_SC = OFF_VF + NV * F16;   // [NS][128] float: key factors, value scales
-  static constexpr int OFF_BAR = OFF_SC + NS * 128 * 4;
-  static constexpr int NBAR = 2 * NR + 2 * NK + 2 * NV + 2 * NS + 3 * NSB + 3;
+  static constexpr int OFF_SC = OFF_VF + NV * F16;   // [NS][2 TK] float: key factors, value scales
+  static constexpr int OFF_BAR = OFF_SC + NS * 2 * TK * 4;
+  static constexpr int NBAR = 2 * NR + 2 * NK + 2 * NV + NS + 3 * NSB + 3;
   // at least half of the SM's shared memory: one CTA per SM owns all 512 TMEM columns
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 128 + 1024;
   static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
-  static constexpr uint32_t COL_S = 0, COL_Q = 64 * NSB, COL_O = 256;
-  static_assert(COL_Q + D / 2 <= COL_O && COL_O + D <= 512, "TMEM columns");
-  static constexpr uint32_t ID_S = tc::idesc_f16(128, 64, false, false);
+  // TMEM columns: S buffers from 0, the O accumulator at 256, Q in the gap
+  // below 256 when it fits there, else right after O
+  static constexpr uint32_t COL_S = 0, COL_O = 256;
+  static constexpr uint32_t COL_Q = TK * NSB + D / 2 <= 256 ? TK * NSB : 256 + D;
+  static_assert(COL_O + D <= 512 && COL_Q + D / 2 <= 512 && TK * NSB <= 256, "TMEM columns");
+  static constexpr uint32_t ID_S = tc::idesc_f16(128, TK, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
   static constexpr float THR = KV == KIND_FP8 ? 0.f : 8.f;  // exact maximum when P carries V scales
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-  static_assert(UPT * 32 * NDW == 4 * D, "units per tile");
+  static_assert(RPT * (D / 8) == 32 * NDW && PASSES * RPT == 64 && RPT % 8 == 0, "unit map");
 };
 
 // Four E4M3 codes -> two f16x2 (exact).
@@ -94,64 +99,64 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t& h0, uint32_t& h
 // softmax warps' 16x256b stores lay out P.
 __device__ __forceinline__ int vrow(int r) { return (r & ~15) | ((r & 6) << 1) | ((r & 8) >> 2) | (r & 1); }
 
-// Shared-memory offsets of unit u of a page tile: 16 consecutive dims
-// [16 q, 16 q + 16) of key r (u = r * D / 16 + q), in the raw code / scale
-// tile and in the 128-byte-swizzled K-major f16 tile the MMA reads (64-dim
-// halves of 64 rows x 128 bytes).
-struct DqOff {
-  int src, sc, dst0, dst1, key;
+// One 8-code unit: dims [8 p, 8 p + 8) of one key.  The raw bytes of all of
+// a thread's units are loaded first (RawUnit), then converted to 8 exact f16
+// values each and stored, so that the shared-memory loads are not ordered
+// behind the stores of earlier units.
+struct RawUnit {
+  uint32_t w0, w1, s;  // FP8: 8 codes in w0, w1; NVFP4: 8 codes in w0 and the E4M3 scale byte in s
 };
 
-template <int KIND, int D, bool PERM>
-__device__ __forceinline__ DqOff dq_offsets(int u) {
-  constexpr int CB = code_row_bytes<KIND>(D), RB = CB < 128 ? CB : 128, SB = scale_row_bytes<KIND>(D);
-  const int r = u / (D / 16), q = u % (D / 16);
-  const int col = KIND == KIND_FP8 ? 16 * q : 8 * q;
-  const int row = PERM ? vrow(r) : r;
-  DqOff o;
-  o.src = (col / RB) * (64 * RB) + static_cast<int>(swz<RB>(r, col % RB));
-  o.sc = r * SB + q;
-  o.dst0 = (q / 4) * 8192 + static_cast<int>(swz<128>(row, (q % 4) * 32));
-  o.dst1 = (q / 4) * 8192 + static_cast<int>(swz<128>(row, (q % 4) * 32 + 16));
-  o.key = r;
-  return o;
+template <int KIND>
+__device__ __forceinline__ RawUnit ld_unit(const uint8_t* src, const uint8_t* sc) {
+  RawUnit u;
+  if constexpr (KIND == KIND_FP8) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    u.w0 = w.x;
+    u.w1 = w.y;
+    u.s = 0u;
+  } else {
+    u.w0 = *reinterpret_cast<const uint32_t*>(src);
+    u.w1 = 0u;
+    u.s = *sc;
+  }
+  return u;
 }
 
-// One unit: 16 codes to 16 exact f16 values (zero when the key lies past the
-// frontier).
+// Converts a unit and stores its 16 bytes of f16; zero when the key lies past
+// the frontier or the tile's pages.
 template <int KIND>
-__device__ __forceinline__ void deq(const uint8_t* codes, const uint8_t* scales, uint8_t* tile, const DqOff& o,
-                                    bool zero) {
-  uint32_t h[8];
+__device__ __forceinline__ void cvt_unit(const RawUnit& u, uint8_t* dst, bool zero) {
+  uint32_t h[4];
   if (zero) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = 0u;
+    for (int i = 0; i < 4; ++i) h[i] = 0u;
   } else if constexpr (KIND == KIND_FP8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(codes + o.src);
-    e4m3x4_f16(w.x, h[0], h[1]);
-    e4m3x4_f16(w.y, h[2], h[3]);
-    e4m3x4_f16(w.z, h[4], h[5]);
-    e4m3x4_f16(w.w, h[6], h[7]);
+    e4m3x4_f16(u.w0, h[0], h[1]);
+    e4m3x4_f16(u.w1, h[2], h[3]);
   } else {
-    const uint2 w = *reinterpret_cast<const uint2*>(codes + o.src);
-    const uint32_t sbyte = scales[o.sc];
-    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(sbyte * 0x101u));  // the scale in both halves
-    e2m1x8_f16(w.x, h[0], h[1], h[2], h[3]);
-    e2m1x8_f16(w.y, h[4], h[5], h[6], h[7]);
+    const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(u.s * 0x101u));  // the scale in both halves
+    e2m1x8_f16(u.w0, h[0], h[1], h[2], h[3]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = hmul2_u32(h[i], s2);
+    for (int i = 0; i < 4; ++i) h[i] = hmul2_u32(h[i], s2);
   }
-  *reinterpret_cast<uint4*>(tile + o.dst0) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(tile + o.dst1) = make_uint4(h[4], h[5], h[6], h[7]);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-// True in one lane of the (converged) warp.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(pred));
-  return pred != 0;
+// Byte offsets of a thread's first unit (row r0, column unit p) in a raw page
+// stage and in the f16 tile (row `frow` of the tile); the other units of the
+// thread follow at fixed strides, as RPT is a multiple of 8 (the swizzle
+// phase of the row does not change).
+template <int KIND, int D>
+__device__ __forceinline__ int raw_off(int r0, int p) {
+  constexpr int CB = code_row_bytes<KIND>(D), RB = CB < 128 ? CB : 128;
+  const int col = KIND == KIND_FP8 ? 8 * p : 4 * p;
+  return (col / RB) * (64 * RB) + static_cast<int>(swz<RB>(r0, col % RB));
+}
+
+template <int TK>
+__device__ __forceinline__ int f16_off(int frow, int p) {
+  return (p / 8) * (TK * 128) + static_cast<int>(swz<128>(frow, (p % 8) * 16));
 }
 
 __device__ __forceinline__ void v_arrive(uint64_t* bar) {
@@ -162,8 +167,8 @@ template <int KK, int KV, int D>
 __global__ void __launch_bounds__(448, 1)
     vdecode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, DecodeArgs a) {
   using Cfg = VCfg<KK, KV, D>;
-  constexpr int NR = Cfg::NR, NK = Cfg::NK, NV = Cfg::NV, NS = Cfg::NS, NDW = Cfg::NDW;
-  constexpr int NSB = Cfg::NSB, LA = Cfg::LA;
+  constexpr int NR = Cfg::NR, NK = Cfg::NK, NV = Cfg::NV, NS = Cfg::NS, NDW = Cfg::NDW, NSB = Cfg::NSB;
+  constexpr int TK = Cfg::TK, PPT = Cfg::PPT;
   constexpr int R = 32;  // query rows of a part in the workspace
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,17 +176,16 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t* sVf = smem + Cfg::OFF_VF;
   float* sSc = reinterpret_cast<float*>(smem + Cfg::OFF_SC);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  uint64_t* raw_full = bars;
+  uint64_t* raw_full = bars;             // [NR] raw page stages
   uint64_t* raw_empty = raw_full + NR;
-  uint64_t* kf_full = raw_empty + NR;
+  uint64_t* kf_full = raw_empty + NR;    // [NK] f16 K tiles
   uint64_t* kf_empty = kf_full + NK;
-  uint64_t* vf_full = kf_empty + NK;
+  uint64_t* vf_full = kf_empty + NK;     // [NV] f16 V tiles
   uint64_t* vf_empty = vf_full + NV;
-  uint64_t* sc_full = vf_empty + NV;
-  uint64_t* sc_empty = sc_full + NS;
-  uint64_t* s_full = sc_empty + NS;     // [NSB]: S(j) in buffer j % NSB
-  uint64_t* p_full = s_full + NSB;      // [NSB]: P(j) written over it
-  uint64_t* o_done = p_full + NSB;      // [NSB]: P V(j) accumulated
+  uint64_t* sc_full = vf_empty + NV;     // [NS] key factors / value scales of a tile
+  uint64_t* s_full = sc_full + NS;       // [NSB]: S(j) in buffer j % NSB
+  uint64_t* p_full = s_full + NSB;       // [NSB]: P(j) written over it
+  uint64_t* o_done = p_full + NSB;       // [NSB]: P V(j) accumulated
   uint64_t* q_ready = o_done + NSB;
   uint64_t* app = q_ready + 1;
   uint64_t* drain = app + 1;
@@ -205,10 +209,7 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&vf_full[i], NDW);
       mbar_init(&vf_empty[i], 1);
     }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&sc_full[i], NDW);
-      mbar_init(&sc_empty[i], 4);
-    }
+    for (int i = 0; i < NS; ++i) mbar_init(&sc_full[i], NDW);
     for (int i = 0; i < NSB; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(448, 1)
   }
   const int F = b >= 0 ? s_F[b] : 0;
   const int p0 = split * chunk;
-  const int n = b >= 0 ? min(chunk, npages - p0) : 0;
+  const int n = b >= 0 ? min(chunk, npages - p0) : 0;  // pages of this CTA
+  const int nt = (n + PPT - 1) / PPT;                  // key tiles
   const int app_lo = early ? (F - a.T) >> 6 : 0x7fffffff;
   const int R_real = a.T * a.G;
   const int32_t* trow = a.tables + static_cast<int64_t>(b >= 0 ? s_row[b] : 0) * a.L;
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(448, 1)
   if (b < 0) {
     // no work: only the TMEM allocation is released below
   } else if (warp == 12) {
-    // -------------------- TMA producer of raw code / scale tiles --------------------
+    // -------------------- TMA producer of raw code / scale pages --------------------
     if (lane == 0) {
       bool app_seen = false;
       int issued = 0;
@@ -314,41 +316,42 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp == 13) {
     // ------------------------------ MMA issuer --------------------------------
     // The whole warp runs the loop, so the operand descriptors are warp-uniform
-    // values; one elected lane issues the MMAs and commits.
+    // values; lane 0 issues every MMA and commit, so a commit covers all MMAs
+    // issued before it.
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(q_ready, 0, a.status));
     tc::fence_after();
     const uint32_t k_base = smem_u32(sKf), v_base = smem_u32(sVf);
-    // issue order S(0) .. S(LA - 1), then S(j), P V(j - LA) for every j
-    for (int j = 0; ok && j < n + LA; ++j) {
-      if (j < n) {
+    // issue order S(0), then S(j), P V(j - 1) for every tile j
+    for (int j = 0; ok && j < nt + 1; ++j) {
+      if (j < nt) {
         const int ks = j % NK, sb = j % NSB;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&kf_full[ks], (j / NK) & 1, a.status) && !*s_abort);
         if (!ok) break;
         tc::fence_after();
         const uint64_t kd = tc::smem_desc(k_base + ks * Cfg::F16, 16, 1024);
-        const uint32_t sd = tmem + Cfg::COL_S + 64 * sb;
-        if (elect_one()) {
+        const uint32_t sd = tmem + Cfg::COL_S + TK * sb;
+        if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             tc::mma_ts(sd, tmem + Cfg::COL_Q + kk * 8,
-                       kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
+                       kd + static_cast<uint64_t>(((kk >> 2) * Cfg::CHUNK + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
           tc::commit(&s_full[sb]);
           tc::commit(&kf_empty[ks]);
         }
         __syncwarp();
       }
-      if (j >= LA) {
-        const int jj = j - LA, vs = jj % NV, pb = jj % NSB;
+      if (j >= 1) {
+        const int jj = j - 1, vs = jj % NV, pb = jj % NSB;
         ok = mbar_wait_bounded(&vf_full[vs], (jj / NV) & 1, a.status) && !*s_abort;
         if (ok) ok = mbar_wait_bounded(&p_full[pb], (jj / NSB) & 1, a.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after();
-        const uint64_t vd = tc::smem_desc(v_base + vs * Cfg::F16, 8192, 1024);
-        const uint32_t pa = tmem + Cfg::COL_S + 64 * pb;
-        if (elect_one()) {
+        const uint64_t vd = tc::smem_desc(v_base + vs * Cfg::F16, Cfg::CHUNK, 1024);
+        const uint32_t pa = tmem + Cfg::COL_S + TK * pb;
+        if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < TK / 16; ++kk)
             tc::mma_ts(tmem + Cfg::COL_O, pa + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), Cfg::ID_O,
                        (jj > 0 || kk > 0));
           tc::commit(&o_done[pb]);
@@ -365,12 +368,12 @@ __global__ void __launch_bounds__(448, 1)
     // ----------------- dequantize warps (and the fused append) ------------------
     const int dw = warp - 4;          // 0..7
     const int dt = dw * 32 + lane;    // 0..255
-    DqOff ko[Cfg::UPT], vo[Cfg::UPT];
-#pragma unroll
-    for (int k = 0; k < Cfg::UPT; ++k) {
-      ko[k] = dq_offsets<KK, D, false>(dt + 256 * k);
-      vo[k] = dq_offsets<KV, D, true>(dt + 256 * k);
-    }
+    const int pu = dt % (D / 8), r0 = dt / (D / 8);
+    const int k_src = raw_off<KK, D>(r0, pu), v_src = raw_off<KV, D>(r0, pu);
+    const int k_dst = f16_off<TK>(r0, pu);
+    // V rows are permuted inside 16-row groups: with RPT a multiple of 16 the
+    // thread's units still sit at fixed strides from its first one
+    const int v_dst = f16_off<TK>(vrow(r0), pu);
     if (early) griddep_wait();
     if (early) {  // the new tokens whose pages this CTA reads, one warp per token
       constexpr int KCBW = code_row_bytes<KK>(D), VCBW = code_row_bytes<KV>(D);
@@ -392,42 +395,91 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) v_arrive(app);
     }
-    for (int i = 0; i < n; ++i) {
-      const int s = i % NR;
-      bool ok = mbar_wait_bounded(&raw_full[s], (i / NR) & 1, a.status) && !*s_abort;
-      const uint8_t* st = smem + s * Cfg::RAW;
-      const int kvalid = F - 64 * (p0 + i);  // V rows >= kvalid lie past the frontier
-      if (ok && i >= NK) ok = mbar_wait_bounded(&kf_empty[i % NK], ((i / NK) - 1) & 1, a.status);
-      if (ok) {
-        uint8_t* kt = sKf + (i % NK) * Cfg::F16;
+    for (int j = 0; j < nt; ++j) {
+      const int npg = min(PPT, n - PPT * j);                // pages of this tile
+      const int kv_lim = min(F - 64 * (p0 + PPT * j), 64 * npg);  // keys of the tile below the frontier
+      bool ok = true;
+      const uint8_t* st[PPT];
 #pragma unroll
-        for (int k = 0; k < Cfg::UPT; ++k) deq<KK>(st, st + Cfg::R_KSC, kt, ko[k], false);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int pi = 0; pi < PPT; ++pi) {
+        const int i = PPT * j + min(pi, npg - 1);
+        st[pi] = smem + (i % NR) * Cfg::RAW;
+        if (pi < npg && ok) ok = mbar_wait_bounded(&raw_full[i % NR], (i / NR) & 1, a.status) && !*s_abort;
       }
-      __syncwarp();
-      if (lane == 0) v_arrive(&kf_full[i % NK]);
-      if (ok && i >= NV) ok = mbar_wait_bounded(&vf_empty[i % NV], ((i / NV) - 1) & 1, a.status);
-      if (ok) {
-        uint8_t* vt = sVf + (i % NV) * Cfg::F16;
-#pragma unroll
-        for (int k = 0; k < Cfg::UPT; ++k) deq<KV>(st + Cfg::R_KS, st + Cfg::R_VSC, vt, vo[k], vo[k].key >= kvalid);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      __syncwarp();
-      if (lane == 0) v_arrive(&vf_full[i % NV]);
-      if (ok && i >= NS) ok = mbar_wait_bounded(&sc_empty[i % NS], ((i / NS) - 1) & 1, a.status);
-      if (ok && dt < 64) {
-        float* sc = sSc + (i % NS) * 128;
+      // The tile's key factors and value scales first.  Slot j % NS was last
+      // read by the softmax for tile j - NS, which finished before P V(j - NS)
+      // could start; tile j - 1 of this loop waited for P V(j - 1 - NV), a
+      // later one (commits of one issuing thread complete in order).
+      if (ok && dt < TK) {
+        float* sc = sSc + (j % NS) * 2 * TK;
+        const int pi = dt / 64, row = dt % 64;
+        const uint8_t* sp = smem + ((PPT * j + pi) % NR) * Cfg::RAW;  // read only when pi < npg
         float kscale = 1.f, vscale = 1.f;
-        if constexpr (KK == KIND_FP8) kscale = __half2float(*reinterpret_cast<const __half*>(st + Cfg::R_KSC + dt * 2));
-        if constexpr (KV == KIND_FP8) vscale = __half2float(*reinterpret_cast<const __half*>(st + Cfg::R_VSC + dt * 2));
+        if (pi < npg) {
+          if constexpr (KK == KIND_FP8)
+            kscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_KSC + row * 2));
+          if constexpr (KV == KIND_FP8)
+            vscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_VSC + row * 2));
+        }
         sc[dt] = kscale * a.softmax_scale * kLog2e;
-        sc[64 + dt] = dt < kvalid ? vscale : 0.f;
+        sc[TK + dt] = dt < kv_lim ? vscale : 0.f;
       }
+      __syncwarp();
+      if (lane == 0) v_arrive(&sc_full[j % NS]);
+      // K buffer j % NK held tile j - NK, whose S was issued before
+      // P V(j - NK - 1), which tile j - 1 of this loop waited for; only tile
+      // NK has no such earlier wait
+      static_assert(NS >= NV + 1 && NK == NV, "the waits these orderings rely on");
+      if (ok && j == NK) ok = mbar_wait_bounded(&kf_empty[0], 0, a.status);
+      if (ok) {
+        uint8_t* kt = sKf + (j % NK) * Cfg::F16;
+        RawUnit ru[PPT * Cfg::PASSES];
+#pragma unroll
+        for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+          for (int k = 0; k < Cfg::PASSES; ++k)
+            if (pi < npg)  // keys of a missing page are masked in the softmax
+              ru[pi * Cfg::PASSES + k] =
+                  ld_unit<KK>(st[pi] + k_src + Cfg::RPT * k * Cfg::K_RB,
+                              st[pi] + Cfg::R_KSC + (r0 + Cfg::RPT * k) * Cfg::KSB + pu / 2);
+#pragma unroll
+        for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+          for (int k = 0; k < Cfg::PASSES; ++k)
+            if (pi < npg) cvt_unit<KK>(ru[pi * Cfg::PASSES + k], kt + k_dst + 64 * pi * 128 + Cfg::RPT * k * 128, false);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) v_arrive(&kf_full[j % NK]);
+      if (ok && j >= NV) ok = mbar_wait_bounded(&vf_empty[j % NV], ((j / NV) - 1) & 1, a.status);
+      if (ok) {
+        uint8_t* vt = sVf + (j % NV) * Cfg::F16;
+        RawUnit ru[PPT * Cfg::PASSES];
+#pragma unroll
+        for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+          for (int k = 0; k < Cfg::PASSES; ++k)
+            if (64 * pi + r0 + Cfg::RPT * k < kv_lim)
+              ru[pi * Cfg::PASSES + k] =
+                  ld_unit<KV>(st[pi] + Cfg::R_KS + v_src + Cfg::RPT * k * Cfg::V_RB,
+                              st[pi] + Cfg::R_VSC + (r0 + Cfg::RPT * k) * Cfg::VSB + pu / 2);
+#pragma unroll
+        for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+          for (int k = 0; k < Cfg::PASSES; ++k) {
+            const int key = 64 * pi + r0 + Cfg::RPT * k;
+            const int off = Cfg::RPT % 16 == 0 ? v_dst + (64 * pi + Cfg::RPT * k) * 128 : f16_off<TK>(vrow(key), pu);
+            cvt_unit<KV>(ru[pi * Cfg::PASSES + k], vt + off, key >= kv_lim);
+          }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) v_arrive(&vf_full[j % NV]);
       __syncwarp();
       if (lane == 0) {
-        v_arrive(&sc_full[i % NS]);
-        v_arrive(&raw_empty[s]);
+#pragma unroll
+        for (int pi = 0; pi < PPT; ++pi)
+          if (pi < npg) v_arrive(&raw_empty[(PPT * j + pi) % NR]);
       }
       if (!ok) {
         *s_abort = 1;
@@ -436,7 +488,8 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else {
     // ---------- softmax and output: warp w owns query rows [8 w, 8 w + 8) ----------
-    const int s4 = lane & 3, rl = lane >> 2;  // this thread: row rl of the quadrant, keys 8k + 2 s4 + {0, 1}
+    constexpr int NREP = TK / 8;                // 16x256b repetitions of a tile's S: 8 keys each
+    const int s4 = lane & 3, rl = lane >> 2;    // this thread: row rl of the quadrant, keys 8k + 2 s4 + {0, 1}
     const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
     const int qr = 8 * warp + rl;
     const bool row_real = qr < R_real;
@@ -484,7 +537,7 @@ __global__ void __launch_bounds__(448, 1)
     const float rs = __shfl_sync(0xffffffffu, rs_q, rl);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < nt; ++j) {
       const int sb = j % NSB, ss = j % NS;
       ok = mbar_wait_bounded(&s_full[sb], (j / NSB) & 1, a.status) && !*s_abort;
       if (ok) ok = mbar_wait_bounded(&sc_full[ss], (j / NS) & 1, a.status) && !*s_abort;
@@ -494,40 +547,46 @@ __global__ void __launch_bounds__(448, 1)
         break;
       }
       tc::fence_after();
-      float x[16];
+      float x[2 * NREP];
       {
-        uint32_t v[32];
-        tc::ld16x256_x8(tmem + lb + Cfg::COL_S + 64 * sb, v);
+        uint32_t v[NREP / 8][32];
+#pragma unroll
+        for (int hh = 0; hh < NREP / 8; ++hh) tc::ld16x256_x8(tmem + lb + Cfg::COL_S + TK * sb + 64 * hh, v[hh]);
         tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          x[2 * k] = __uint_as_float(v[4 * k]);
-          x[2 * k + 1] = __uint_as_float(v[4 * k + 1]);
-        }
-      }
-      const float* ksc = sSc + ss * 128 + 2 * s4;  // + 8 k: factors of keys 8k + 2 s4 + {0, 1}
-      const int key0 = 64 * (p0 + j) + 2 * s4;
-      if (64 * (p0 + j) + 63 <= F - a.T) {  // every key of the page is visible to every row
+        for (int hh = 0; hh < NREP / 8; ++hh)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 8; ++k) {
+            x[16 * hh + 2 * k] = __uint_as_float(v[hh][4 * k]);
+            x[16 * hh + 2 * k + 1] = __uint_as_float(v[hh][4 * k + 1]);
+          }
+      }
+      const float* ksc = sSc + ss * 2 * TK + 2 * s4;  // + 8 k: factors of keys 8k + 2 s4 + {0, 1}
+      const int kt0 = 64 * (p0 + PPT * j);
+      const int key_end = 64 * (p0 + min(PPT * j + PPT, n));  // keys of this CTA in the tile end here
+      if (kt0 + TK - 1 <= F - a.T && kt0 + TK <= key_end) {  // every key visible to every row
+#pragma unroll
+        for (int k = 0; k < NREP; ++k) {
           const float2 kf = *reinterpret_cast<const float2*>(ksc + 8 * k);
           x[2 * k] = row_real ? x[2 * k] * kf.x : -INFINITY;
           x[2 * k + 1] = row_real ? x[2 * k + 1] * kf.y : -INFINITY;
         }
       } else {
-        const int kmax = row_real ? lim - key0 : -1;
+        const int kmax = row_real ? min(lim, key_end - 1) - (kt0 + 2 * s4) : -1;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < NREP; ++k) {
           const float2 kf = *reinterpret_cast<const float2*>(ksc + 8 * k);
           x[2 * k] = 8 * k <= kmax ? x[2 * k] * kf.x : -INFINITY;
           x[2 * k + 1] = 8 * k + 1 <= kmax ? x[2 * k + 1] * kf.y : -INFINITY;
         }
       }
-      // row maximum: a tree over this thread's 16 keys, then over the row's 4 threads
-      float mt[4];
+      // row maximum: a tree over this thread's keys, then over the row's 4 threads
+      float mt[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) mt[u] = fmaxf(fmaxf(x[u], x[u + 4]), fmaxf(x[u + 8], x[u + 12]));
-      float pm = fmaxf(fmaxf(mt[0], mt[1]), fmaxf(mt[2], mt[3]));
+      for (int u = 0; u < 8; ++u) mt[u] = x[u];
+#pragma unroll
+      for (int u = 8; u < 2 * NREP; ++u) mt[u & 7] = fmaxf(mt[u & 7], x[u]);
+      float pm = fmaxf(fmaxf(fmaxf(mt[0], mt[1]), fmaxf(mt[2], mt[3])), fmaxf(fmaxf(mt[4], mt[5]), fmaxf(mt[6], mt[7])));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
       const float rmax = pm == -INFINITY ? -INFINITY : pm * rs;
@@ -540,15 +599,15 @@ __global__ void __launch_bounds__(448, 1)
         resc = true;
       }
       const float mu = m_used == -INFINITY ? 0.f : m_used;
-      uint32_t pk[16];
+      uint32_t pk[NREP * 2];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < NREP; ++k) {
         float p0v = ex2(fmaf(x[2 * k], rs, -mu));
         float p1v = ex2(fmaf(x[2 * k + 1], rs, -mu));
         ps[k & 3] += p0v + p1v;
         if constexpr (KV == KIND_FP8) {
-          const float2 vf = *reinterpret_cast<const float2*>(ksc + 64 + 8 * k);
+          const float2 vf = *reinterpret_cast<const float2*>(ksc + TK + 8 * k);
           p0v *= vf.x;
           p1v *= vf.y;
         }
@@ -556,13 +615,11 @@ __global__ void __launch_bounds__(448, 1)
         pk[4 * (k >> 1) + (k & 1)] = pack_f16x2(p0v, p1v);
       }
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {  // lanes 8..15 of the quadrant: zero rows
+      for (int jj = 0; jj < NREP / 2; ++jj) {  // lanes 8..15 of the quadrant: zero rows
         pk[4 * jj + 2] = 0u;
         pk[4 * jj + 3] = 0u;
       }
       l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      __syncwarp();
-      if (lane == 0) v_arrive(&sc_empty[ss]);
       // O is rescaled only when a row's maximum moved: then P V(j - 1) must
       // have landed first (P V(j - 1 - NSB) has, as S(j) has completed, so
       // the parity of o_done[(j - 1) % NSB] is unambiguous); P V(j) waits
@@ -589,7 +646,11 @@ __global__ void __launch_bounds__(448, 1)
           tc::st16x256_x8(tmem + lb + Cfg::COL_O + c0, ov);
         }
       }
-      tc::st16x256_x4(tmem + lb + Cfg::COL_S + 64 * sb, pk);
+      if constexpr (TK == 128) {
+        tc::st16x256_x8(tmem + lb + Cfg::COL_S + TK * sb, pk);
+      } else {
+        tc::st16x256_x4(tmem + lb + Cfg::COL_S + TK * sb, pk);
+      }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
