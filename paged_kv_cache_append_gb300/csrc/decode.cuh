@@ -884,7 +884,6 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
   __shared__ int s_F[8];
   __shared__ float2 sml[R * kMaxSplits];
   __shared__ float sw[R * kMaxSplits];
-  __shared__ float4 sacc[4][R * 8];
   const int b = blockIdx.x, h = blockIdx.y, d0 = blockIdx.z * 32, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < a.B) {
@@ -906,6 +905,23 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
   if (nsplit <= 1) return;  // the decode wrote this row's output
   const int R_real = a.T * a.G;
   const int64_t part0 = (static_cast<int64_t>(b) * a.H + h) * a.target;
+  // item = (query row, 4 dims of the slice); four threads share an item and
+  // take every fourth split, all of their loads in flight together.  The
+  // accumulators of a thread's first item are loaded before the (m, l)
+  // weights are known, so the two reads overlap.
+  const int sub = tid & 3;
+  const int64_t stride = static_cast<int64_t>(R) * D / 4;
+  auto load_item = [&](int item, float4 (&v)[kMaxSplits / 4]) {
+    const int qr = item >> 3, d = d0 + (item & 7) * 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (part0 * R + qr) * D + d);
+#pragma unroll
+    for (int u = 0; u < kMaxSplits / 4; ++u) {
+      const int k = sub + 4 * u;
+      v[u] = k < nsplit ? __ldcg(src + k * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  float4 v[kMaxSplits / 4];
+  if ((tid >> 2) < R_real * 8) load_item(tid >> 2, v);
   for (int x = tid; x < R_real * nsplit; x += 256) {
     const int qr = x / nsplit, k = x - qr * nsplit;
     sml[x] = __ldcg(&a.ws_ml[(part0 + k) * R + qr]);
@@ -927,20 +943,10 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  // item = (query row, 4 dims of the slice); four threads share an item and
-  // take every fourth split, all of their loads in flight together
-  const int sub = tid & 3;
   for (int item = tid >> 2; item < R_real * 8; item += 64) {
+    if (item != (tid >> 2)) load_item(item, v);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int qr = item >> 3, d = d0 + (item & 7) * 4;
-    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (part0 * R + qr) * D + d);
-    const int64_t stride = static_cast<int64_t>(R) * D / 4;
-    float4 v[kMaxSplits / 4];
-#pragma unroll
-    for (int u = 0; u < kMaxSplits / 4; ++u) {
-      const int k = sub + 4 * u;
-      v[u] = k < nsplit ? __ldcg(src + k * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const int qr = item >> 3;
 #pragma unroll
     for (int u = 0; u < kMaxSplits / 4; ++u) {
       const int k = sub + 4 * u;
@@ -950,23 +956,20 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
       acc.z = fmaf(w, v[u].z, acc.z);
       acc.w = fmaf(w, v[u].w, acc.w);
     }
-    sacc[sub][item] = acc;
-  }
-  __syncthreads();
-  for (int item = tid; item < R_real * 8; item += 256) {  // the four shares in a fixed order
-    float4 r = sacc[0][item];
+    // the four shares (lanes 4k .. 4k + 3) in a fixed order: (0 + 1) + (2 + 3)
 #pragma unroll
-    for (int u = 1; u < 4; ++u) {
-      const float4 x = sacc[u][item];
-      r.x += x.x;
-      r.y += x.y;
-      r.z += x.z;
-      r.w += x.w;
+    for (int off = 1; off < 4; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
     }
-    const int qr = item >> 3, d = d0 + (item & 7) * 4;
-    const int t = qr / a.G, g = qr % a.G;
-    __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(r.x, r.y), pack_bf16x2(r.z, r.w));
+    if (sub == 0) {
+      const int d = d0 + (item & 7) * 4;
+      const int t = qr / a.G, g = qr % a.G;
+      __nv_bfloat16* dst = a.out + ((static_cast<int64_t>(b) * a.T + t) * a.Hq + h * a.G + g) * D + d;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
   }
 }
 
