@@ -203,8 +203,13 @@ int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t
  * Kernels are launched with programmatic stream serialization (they may start
  * while the previous kernel in the stream drains, and read nothing before it
  * completes).
- * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T*Hq/H > 64),
- * NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
+ * R = T * Hq / H query rows per KV head: R <= 16 runs a warp-level tensor-core
+ * kernel for every profile; 17 <= R <= 32 over FP8-row, NVFP4-G16 and K8V4
+ * pools runs a 5th-generation tensor-core kernel (csrc/vdecode.cu), and over
+ * BF16 and INT8-G64 pools the warp-level kernel at head_dim 64 and 128.
+ * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T < 1),
+ * NK_ERR_UNSUPPORTED (R > 32, or R > 16 at head_dim 256 over BF16 or
+ * INT8-G64 pools), NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
 int nk_paged_decode_attention(const void* q, int32_t Hq, const nk_pool* pool, int32_t layer,
                               const int32_t* block_tables, const int32_t* table_rows,
                               const int32_t* frontiers, int32_t B, int32_t T,
@@ -298,8 +303,9 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
                                size_t* bytes);
 
 /* Chunked prefill / replay attention through the block tables (BF16, FP8-row,
- * NVFP4-G16 and K8V4 pools; quantized pages are dequantized inside the
- * kernel, with f16 tensor-core operands that hold the codes exactly).
+ * NVFP4-G16 and K8V4 pools; quantized pages are first converted by their own
+ * launch into f16 tiles that hold the codes exactly, which the tensor-core
+ * launch then reads).
  * Query i < chunk_len[b] of row b sits at logical position prefix_len[b] + i
  * and attends keys j <= prefix_len[b] + i; the chunk's own K/V must already
  * be appended.  Prefill work is proportional to prefix*S + S(S+1)/2 query-key
