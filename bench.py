@@ -92,8 +92,8 @@ def make_workload(name, layers=None, context=None):
         return W.k8v4_long(T=4, **kw)
     if name == "tiny_bf16":
         return W.tiny_bf16()
-    if name in ("fp8_prefill", "k8v4_prefill", "nvfp4_prefill"):
-        return W.bf16_prefill(profile={"fp8_prefill": "fp8_row", "k8v4_prefill": "k8v4",
+    if name in ("int8_prefill", "fp8_prefill", "k8v4_prefill", "nvfp4_prefill"):
+        return W.bf16_prefill(profile={"int8_prefill": "int8_g64", "fp8_prefill": "fp8_row", "k8v4_prefill": "k8v4",
                                        "nvfp4_prefill": "nvfp4_g16"}[name], **kw)
     return W.WORKLOADS[name](**kw)
 
@@ -687,7 +687,7 @@ def main():
     ap.add_argument("--impl", default="nk", choices=["nk", "reference"])
     ap.add_argument("--workload", default="int8_decode",
                     choices=["tiny_bf16", "int8_decode", "fp8_shared", "k8v4_long", "k8v4_verify",
-                             "bf16_prefill", "fp8_prefill", "k8v4_prefill", "nvfp4_prefill"])
+                             "bf16_prefill", "int8_prefill", "fp8_prefill", "k8v4_prefill", "nvfp4_prefill"])
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling)")
     ap.add_argument("--context", type=int, default=None, help="smaller max context S (profiling)")
     ap.add_argument("--no-sweep", action="store_true")

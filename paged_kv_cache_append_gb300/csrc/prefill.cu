@@ -424,8 +424,6 @@ extern "C" int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const
   if (!q_chunk || !pool || !block_tables || !table_rows || !prefix_len || !chunk_len || !out)
     return fail(NK_ERR_INVALID_ARG, "null argument to nk_paged_prefill_attention");
   if (!std::isfinite(softmax_scale)) return fail(NK_ERR_INVALID_ARG, "softmax_scale is not finite");
-  if (pool->desc.profile == NK_INT8_G64)
-    return fail(NK_ERR_UNSUPPORTED, "chunked prefill is built for BF16, FP8-row, NVFP4-G16 and K8V4 pools");
   const int D = pool->desc.head_dim, H = pool->desc.num_kv_heads;
   if (D != 64 && D != 128 && D != 256) return fail(NK_ERR_UNSUPPORTED, "chunked prefill needs head_dim 64, 128 or 256");
   if (layer < 0 || layer >= pool->desc.num_layers) return fail(NK_ERR_SHAPE, "layer out of range");

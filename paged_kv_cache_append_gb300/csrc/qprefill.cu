@@ -1,6 +1,6 @@
 // qprefill.cu -- chunked prefill / replay attention over quantized pages on
-// the 5th-generation tensor cores: FP8-E4M3FN-row256, NVFP4-G16 and K8V4
-// (FP8-row K, NVFP4 V) pools.
+// the 5th-generation tensor cores: INT8-G64, FP8-E4M3FN-row256, NVFP4-G16 and
+// K8V4 (FP8-row K, NVFP4 V) pools.
 //
 // Two launches, split by what bounds them:
 //   1. qdequant_kernel (HBM bound) converts each page of the prefill rows
@@ -25,9 +25,17 @@
 //     max|q| 2^-31; the scores divide 2^e back out in fp32.
 // With FP8-row V the weights p * s_key must stay finite in f16, so the running
 // maximum is exact (p <= 1); NVFP4 V keeps the lazy 2^8 rescale threshold.
-// INT8-G64 K would need one fp32 accumulator per 64-dim group of each key
-// (its products are not exact in f16); that does not fit the 512 TMEM
-// columns, so INT8-G64 pools are not served here.
+// INT8-G64 is the one profile whose dequantized values are not exact in f16:
+// an INT8 code (7 bits) times its binary16 group scale (11 bits) needs up to
+// 18 significant bits, and an exact form would need one fp32 accumulator per
+// 64-dim group of each key, four times the S columns of tensor memory.  Its
+// pages are dequantized as code * s_g computed exactly in fp32 and rounded
+// once to f16 (relative error <= 2^-11 per element), after a per-key power
+// of two 2^-e, e in [0, 7], that keeps the largest element of the key below
+// 2^15; 2^e goes into the key's fp32 factor (K) or its softmax weight (V),
+// which stays below 2^8 * 2^7 under the lazy 2^8 threshold.  Scores then
+// differ from the exact ones by at most 2^-11 of sum_d |q_d k_d| times the
+// softmax scale, well inside the attention tolerances.
 //
 // Scratch (the call's workspace): K f16 [B][H][L][64][D], V f16 likewise,
 // scales fp32 [B][H][L][128] (64 K scales times softmax_scale * log2 e, then
@@ -87,10 +95,32 @@ __device__ __forceinline__ bool q_row(const QArgs& a, int b, int& row, int& pref
            static_cast<int64_t>(prefix) + chunk > static_cast<int64_t>(a.L) * 64);
 }
 
-// 8 dims [d, d + 8) of one token-head row -> 8 exact f16 values (16 bytes).
+// INT8-G64 rows: the power of two e (0..7) with 127 * max_g s_g * 2^-e < 2^15.
+template <int D>
+__device__ __forceinline__ int int8_row_shift(const uint8_t* scale_row) {
+  float smax = 0.f;
+#pragma unroll
+  for (int g = 0; g < D / 64; ++g)
+    smax = fmaxf(smax, fabsf(__half2float(*reinterpret_cast<const __half*>(scale_row + 2 * g))));
+  int ex = 0;
+  frexpf(127.f * smax, &ex);  // 127 * smax < 2^ex
+  return min(max(ex - 15, 0), 7);
+}
+
+// 8 dims [d, d + 8) of one token-head row -> 8 f16 values (16 bytes): exact
+// for FP8 and NVFP4; for INT8-G64, code * s_g * 2^-e rounded once.
 template <int KIND, int D>
 __device__ __forceinline__ uint4 dequant8(const uint8_t* code_row, const uint8_t* scale_row, int d) {
-  if constexpr (KIND == KIND_FP8) {
+  if constexpr (KIND == KIND_INT8) {
+    const uint2 w = *reinterpret_cast<const uint2*>(code_row + d);
+    const float sg = ldexpf(__half2float(*reinterpret_cast<const __half*>(scale_row + 2 * (d / 64))),
+                            -int8_row_shift<D>(scale_row));
+    const int8_t* c = reinterpret_cast<const int8_t*>(&w);
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = pack_f16x2(static_cast<float>(c[2 * i]) * sg, static_cast<float>(c[2 * i + 1]) * sg);
+    return make_uint4(h[0], h[1], h[2], h[3]);
+  } else if constexpr (KIND == KIND_FP8) {
     const uint2 w = *reinterpret_cast<const uint2*>(code_row + d);
     return make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
                       e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
@@ -138,8 +168,12 @@ __global__ void __launch_bounds__(128) qdequant_kernel(QArgs a) {
   if (tid < 64) {
     float ksc = 0.f, vsc = 0.f;
     if (tid < kvalid) {
-      ksc = KK == KIND_FP8 ? __half2float(*reinterpret_cast<const __half*>(a.ks + (src + tid) * KSB)) : 1.f;
-      vsc = KV == KIND_FP8 ? __half2float(*reinterpret_cast<const __half*>(a.vs + (src + tid) * VSB)) : 1.f;
+      if constexpr (KK == KIND_FP8) ksc = __half2float(*reinterpret_cast<const __half*>(a.ks + (src + tid) * KSB));
+      else if constexpr (KK == KIND_INT8) ksc = ldexpf(1.f, int8_row_shift<D>(a.ks + (src + tid) * KSB));
+      else ksc = 1.f;
+      if constexpr (KV == KIND_FP8) vsc = __half2float(*reinterpret_cast<const __half*>(a.vs + (src + tid) * VSB));
+      else if constexpr (KV == KIND_INT8) vsc = ldexpf(1.f, int8_row_shift<D>(a.vs + (src + tid) * VSB));
+      else vsc = 1.f;
     }
     float* sc = a.scr.sc + (dst / 64) * 128;
     sc[tid] = ksc * a.scale_log2;
@@ -470,7 +504,7 @@ static cudaError_t launch_qd(int D, const CUtensorMap& tk, const CUtensorMap& tv
 }
 
 size_t qprefill_workspace_bytes(const nk_pool* p, int B) {
-  if (p->desc.profile == NK_BF16 || p->desc.profile == NK_INT8_G64) return 0;
+  if (p->desc.profile == NK_BF16) return 0;
   return QScratch::bytes(B, p->desc.num_kv_heads, p->L, p->desc.head_dim);
 }
 
@@ -521,6 +555,7 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   if (rc) return rc;
   cudaError_t e;
   switch (p->desc.profile) {
+    case NK_INT8_G64: e = launch_qd<KIND_INT8, KIND_INT8>(D, tk, tv, a, s); break;
     case NK_FP8_E4M3_ROW: e = launch_qd<KIND_FP8, KIND_FP8>(D, tk, tv, a, s); break;
     case NK_NVFP4_G16: e = launch_qd<KIND_NVFP4, KIND_NVFP4>(D, tk, tv, a, s); break;
     case NK_K8V4: e = launch_qd<KIND_FP8, KIND_NVFP4>(D, tk, tv, a, s); break;

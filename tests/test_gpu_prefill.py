@@ -32,11 +32,19 @@ def prefill_workload(Hkv, G, D, S, prefixes, chunks, Tc, seed, n_decode=0, layer
                       Tc=Tc, scale=1 / math.sqrt(D), seed=seed + 9000)
 
 
-def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major"):
+def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major", kv_scale=1.0, q_scale=1.0,
+                check=True):
+    """Appends the chunk, runs the prefill on the GPU and (check) compares it
+    with the oracle; returns the GPU (out, lse) on the CPU."""
     sc = Scenario(w, layers=(layer,), oracle=True, order=order)
     dev = "cuda"
     k, v = w.chunk_kv(layer)
     q = w.chunk_q(layer)
+    if kv_scale != 1.0:  # chunk rows only: the prefix stays N(0, 1)
+        k = (k.float() * kv_scale).to(torch.bfloat16)
+        v = (v.float() * kv_scale).to(torch.bfloat16)
+    if q_scale != 1.0:
+        q = (q.float() * q_scale).to(torch.bfloat16)
     rows = torch.from_numpy(w.prefill_rows).to(dev)
     pre = torch.from_numpy(w.prefix_len).to(dev)
     chk = torch.from_numpy(w.chunk_len).to(dev)
@@ -57,6 +65,8 @@ def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major"):
     out, lse = sc.gpu.prefill(layer, q.to(dev), sc.tables_d, rows, pre, chk, w.scale)
     torch.cuda.synchronize()
     out, lse = out.cpu(), lse.cpu()
+    if not check:
+        return out, lse
     qf = OF.bf16_bits_to_f64(bf16_to_bits(q))
     for i, r in enumerate(w.prefill_rows):
         P0, Cn = int(w.prefix_len[i]), int(w.chunk_len[i])
@@ -70,6 +80,7 @@ def run_prefill(w, layer=0, poison=False, sample_rows=None, order="page_major"):
         compare_attention(out[i, toks], lse[i, toks], ref_o, ref_l)
         if Cn < w.Tc:   # rows past the chunk are not written
             assert torch.all(out[i, Cn:] == 0) and torch.all(torch.isneginf(lse[i, Cn:]))
+    return out, lse
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
@@ -129,14 +140,43 @@ def test_quantized_prefill_negative_scale():
     run_prefill(dataclasses.replace(w, scale=-w.scale))
 
 
-def test_int8_prefill_is_rejected():
-    from paged_kv_cache_append_gb300 import nk
-    w = prefill_workload(2, 8, 128, 512, prefixes=[10], chunks=[20], Tc=32, seed=1, profile="int8_g64")
-    sc = Scenario(w, layers=(0,), oracle=False)
-    dev = "cuda"
-    with pytest.raises(nk.NkError):
-        sc.gpu.prefill(0, w.chunk_q(0).to(dev), sc.tables_d, torch.from_numpy(w.prefill_rows).to(dev),
-                       torch.from_numpy(w.prefix_len).to(dev), torch.from_numpy(w.chunk_len).to(dev), w.scale)
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G", [8, 1, 16])
+def test_int8_prefill_small(D, G):
+    """INT8-G64 pages: dequantized to f16 once (code * group scale rounded to
+    f16, the one inexact profile), within the attention tolerances."""
+    w = prefill_workload(2 if G < 16 else 1, G, D, 1024, prefixes=[133, 0], chunks=[300, 77], Tc=320,
+                         seed=D + G + 5, profile="int8_g64")
+    run_prefill(w)
+
+
+def test_int8_prefill_stale_tail_and_negative_scale():
+    import dataclasses
+    w = prefill_workload(2, 8, 256, 1024, prefixes=[100, 37], chunks=[45, 200], Tc=256, seed=17,
+                         profile="int8_g64")
+    run_prefill(w, poison=True)
+    run_prefill(dataclasses.replace(w, scale=-w.scale))
+
+
+def test_int8_prefill_power_of_two_scaling_is_exact():
+    """Keys and values times 2^16 and queries times 2^-16 leave the INT8 codes
+    unchanged and multiply the group scales by 2^16, so rows take the per-key
+    shift (2^-3 before the f16 rounding).  Powers of two commute with every
+    rounding on the way, so the output must be exactly 2^16 times the unscaled
+    one (itself checked against the oracle) and the lse identical."""
+    w = prefill_workload(2, 8, 128, 512, prefixes=[0, 0], chunks=[200, 130], Tc=256, seed=21,
+                         profile="int8_g64")
+    out0, lse0 = run_prefill(w)
+    out1, lse1 = run_prefill(w, kv_scale=2.0 ** 16, q_scale=2.0 ** -16, check=False)
+    assert torch.equal(out1.float(), out0.float() * 2.0 ** 16)
+    assert torch.equal(lse1, lse0)
+
+
+def test_int8_prefill_workload_sampled():
+    """The chunked-prefill workload over INT8-G64 pages at full size, one layer."""
+    w = W.bf16_prefill(num_layers=1, profile="int8_g64")
+    sample = np.array([0, 1, 63, 64, 127, 128, 1000, 1023, 2046, 2047])
+    run_prefill(w, sample_rows=sample)
 
 
 def test_prefill_k8v4_workload_sampled():
