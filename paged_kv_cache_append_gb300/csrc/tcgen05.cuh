@@ -55,6 +55,17 @@ __device__ __forceinline__ void ld32(uint32_t addr, uint32_t (&v)[32]) {
       : "r"(addr));
 }
 
+// Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void ld16(uint32_t addr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(addr));
+}
+
 // Each thread of the warp writes 32 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void st32(uint32_t addr, const uint32_t (&v)[32]) {
   asm volatile(
