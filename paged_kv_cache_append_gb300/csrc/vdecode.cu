@@ -7,8 +7,17 @@
 // writes the final out / lse when its row has one split, else a partial
 // (m, l, acc) that merge_kernel combines.  With 32 query rows the warp-level
 // kernel keeps 128 fp32 accumulators per thread in registers and is bound by
-// its mma.sync issue rate; here S and O live in tensor memory.  A key tile is
-// TK = 128 keys (two pages) at head_dim <= 128, one page at 256:
+// its mma.sync issue rate; here S and O live in tensor memory.  Two forms:
+//
+//   vtdecode_kernel (head_dim 64, 128): S^T = K Q^T and O^T = V^T P^T, the
+//     tile's 128 keys as M and the 32 query rows as N; the keys are
+//     dequantized straight into TMEM (the A operand of S^T).  Described
+//     above the kernel.
+//   vdecode_kernel (head_dim 256): S = Q K^T and O += P V with the query
+//     rows in TMEM lanes and the f16 K tile in shared memory, as below.
+//
+// vdecode_kernel: a key tile is TK = 64 keys (one page) at head_dim 256,
+// 128 keys (two pages) at smaller head_dims:
 //   S = Q K^T   tcgen05.mma M 128 x N TK x K D; Q (f16, each query row scaled
 //               by a power of two) in TMEM, K = the tile dequantized to f16 in
 //               shared memory;
@@ -26,10 +35,10 @@
 // every 16-key group; the dequantizing warps store the V tile's rows in that
 // order (vrow), so P V sums over matching keys.
 //
-// Warps (448 threads): 0-3 softmax and output (one per quadrant), 4-11
-// dequantize key tiles (and, in the fused call, encode the new tokens first),
-// 12 is the TMA producer of raw code / scale pages, 13 issues the MMAs.  All
-// waits are bounded.
+// Warps of both kernels (448 threads): 0-3 softmax and output (one per lane
+// quadrant), 4-11 dequantize tiles (and, in the fused call, encode the new
+// tokens first), 12 is the TMA producer of raw code / scale pages, 13 issues
+// the MMAs.  All waits are bounded.
 #include "decode.cuh"
 #include "tcgen05.cuh"
 
