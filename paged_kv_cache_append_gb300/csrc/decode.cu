@@ -12,6 +12,8 @@ namespace nk {
 
 struct DecodePlan {
   int nqt, R, target, ring_bytes;
+  int ctas = 0;  // CTAs per KV head (grid x)
+  int nseg = 0;  // > 0: pieces per head, several per CTA
   size_t ws_ml_bytes, ws_bytes;
   DecodeFn fn;
 };
@@ -50,6 +52,14 @@ static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
   }
   pl->target = p->num_sms * per_sm / H;
   if (pl->target < 1) pl->target = 1;
+  pl->ctas = pl->target;
+  if (vfn && D <= 128) {
+    // the transposed tcgen05 kernel takes several (row, page range) pieces
+    // per CTA, so that equal rows still fill every SM; a row has at most
+    // kMaxSplits pieces, each with its own partial slot
+    pl->nseg = 4 * pl->ctas;
+    pl->target = pl->nseg < kMaxSplits ? pl->nseg : kMaxSplits;
+  }
   plan_sizes(pl, B, H, D);
   return NK_OK;
 }
@@ -115,6 +125,7 @@ static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t la
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
+  a.nseg = pl.nseg;
   a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   if (k_new) {
     a.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -124,7 +135,7 @@ static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t la
     a.ks_w = np == 4 ? static_cast<uint8_t*>(pool->ptrs[layer * np + 2]) : nullptr;
     a.vs_w = np == 4 ? static_cast<uint8_t*>(pool->ptrs[layer * np + 3]) : nullptr;
   }
-  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.ctas, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return NK_OK;
 }
@@ -185,6 +196,11 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
                                         " bytes of scratch; the static scratch holds " +
                                         std::to_string(max_ws));
     pl.target = static_cast<int>(fit < static_cast<size_t>(pl.target) ? fit : pl.target);
+    if (pl.nseg > 0) {
+      if (pl.nseg > pl.target) pl.nseg = pl.target;  // every row's pieces still fit its slots
+    } else {
+      pl.ctas = pl.target;
+    }
     plan_sizes(&pl, B, H, D);
   }
   DecodeArgs a;
@@ -210,8 +226,9 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.M = pool->M;
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
+  a.nseg = pl.nseg;
   a.head_major = pool->desc.order == NK_HEAD_MAJOR;
-  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.target, a.H), s);
+  cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.ctas, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return NK_OK;
 }

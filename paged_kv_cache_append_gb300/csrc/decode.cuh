@@ -70,7 +70,9 @@ struct DecodeArgs {
   uint8_t* vs_w = nullptr;
   float softmax_scale;
   int B, T, Hq, H, G, L, M, C;
-  int target;    // splits per head the chunking aims at (= maxsplit)
+  int target;    // partial slots per (row, KV head) (= maxsplit); with nseg == 0 also the
+                 // splits per head the chunking aims at, one CTA each
+  int nseg = 0;  // > 0: pieces per head the chunking aims at, several per CTA (vdecode.cu)
   int head_major = 0;  // plane order
 };
 
@@ -898,7 +900,7 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = max(split_chunk(total, a.nseg > 0 ? a.nseg : a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
   const int nsplit = max(1, (((s_F[b] + 63) >> 6) + chunk - 1) / chunk);
   griddep_wait();
   griddep_launch_dependents();

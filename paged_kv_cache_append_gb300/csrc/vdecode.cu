@@ -763,7 +763,7 @@ struct VTCfg {
   static constexpr int QB = 32 * D * 2, QCHUNK = 32 * 128;   // Q: D / 64 chunks of 32 rows x 128 B
   static constexpr int PB = 32 * TK * 2, PCHUNK = 32 * 128;  // P^T: TK / 64 chunks of 32 rows x 128 B
   static constexpr int NK = 2, NV = 2, NS = 4, NSB = 2;
-  static constexpr int FIXED = NV * F16V + QB + NSB * PB + NS * 2 * TK * 4 + 4 * 128 * 4 + 2048;
+  static constexpr int FIXED = NV * F16V + 2 * QB + NSB * PB + NS * 2 * TK * 4 + 4 * 128 * 4 + 2048;
   static constexpr int NR_FIT = (204 * 1024 - FIXED) / RAW;
   static constexpr int NR = NR_FIT > 8 ? 8 : NR_FIT;
   // V tiles first: at D = 64 the M = 128 A operand of O^T also reads the
@@ -772,14 +772,14 @@ struct VTCfg {
   static constexpr int OFF_VF = 0;
   static constexpr int OFF_RAW = NV * F16V;
   static constexpr int OFF_Q = OFF_RAW + NR * RAW;
-  static constexpr int OFF_P = OFF_Q + QB;
+  static constexpr int OFF_P = OFF_Q + 2 * QB;             // Q: two buffers (this piece, the next)
   static constexpr int OFF_SC = OFF_P + NSB * PB;         // [NS][2 TK] float: key factors, value scales
   static constexpr int OFF_MX = OFF_SC + NS * 2 * TK * 4;  // [2][4][32] float: row maxima of each warp
   static constexpr int OFF_L = OFF_MX + 2 * 128 * 4;      // [4][32] float: row sums of each warp
   static constexpr int OFF_MN = OFF_L + 128 * 4;          // [4][32] float: each warp's -(row maxima)
   static constexpr int OFF_FL = OFF_MN + 128 * 4;         // [2][4] int: each warp's "a maximum moved" flag
   static constexpr int OFF_BAR = OFF_FL + 128;
-  static constexpr int NBAR = 2 * NR + 2 * NK + 2 * NV + NS + 3 * NSB + 4 + 4;
+  static constexpr int NBAR = 2 * NR + 2 * NK + 2 * NV + NS + 3 * NSB + 11;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 128 + 1024;
   static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
   static constexpr uint32_t COL_K = 0, COL_S = NK * D / 2, COL_O = COL_S + NSB * 32;
@@ -870,6 +870,34 @@ __device__ __forceinline__ void key_half_f16(const uint8_t* stage, const uint8_t
   }
 }
 
+// One piece of a head's work: pages [p0, p0 + n) of row b, piece k of ns.
+// A head's rows are cut in row order into pieces of `chunk` pages (the plan
+// of decode.cuh with a budget of a.nseg pieces per head); CTA x of gridDim.x
+// takes pieces [x S / gridDim.x, (x + 1) S / gridDim.x) of the S pieces.
+struct VSeg {
+  int b, k, ns, p0, n, F;
+};
+
+__device__ __forceinline__ VSeg vt_seg(int sg, const int* s_F, int B, int chunk) {
+  VSeg r{0, 0, 1, 0, 0, 0};
+  int acc = 0;
+  for (int bb = 0; bb < B; ++bb) {
+    const int np = (s_F[bb] + 63) >> 6;
+    const int ns = max(1, (np + chunk - 1) / chunk);
+    if (sg < acc + ns) {
+      r.b = bb;
+      r.k = sg - acc;
+      r.ns = ns;
+      r.p0 = r.k * chunk;
+      r.n = min(chunk, np - r.p0);
+      r.F = s_F[bb];
+      return r;
+    }
+    acc += ns;
+  }
+  return r;
+}
+
 template <int KK, int KV, int D>
 __global__ void __launch_bounds__(448, 1)
     vtdecode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, DecodeArgs a) {
@@ -881,7 +909,7 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sVf = smem + Cfg::OFF_VF;
   uint8_t* sRaw = smem + Cfg::OFF_RAW;
-  uint8_t* sQ = smem + Cfg::OFF_Q;
+  uint8_t* sQ = smem + Cfg::OFF_Q;  // [2][QB]: the Q of pieces i and i + 1
   uint8_t* sP = smem + Cfg::OFF_P;
   float* sSc = reinterpret_cast<float*>(smem + Cfg::OFF_SC);
   float* sMx = reinterpret_cast<float*>(smem + Cfg::OFF_MX);
@@ -896,15 +924,17 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* vf_full = kf_empty + NK;     // [NV] f16 V tiles
   uint64_t* vf_empty = vf_full + NV;
   uint64_t* sc_full = vf_empty + NV;     // [NS] key factors / value scales of a tile
-  uint64_t* s_full = sc_full + NS;       // [NSB]: S^T(j) in buffer j % NSB
-  uint64_t* p_full = s_full + NSB;       // [NSB]: P^T(j) in shared buffer j % NSB
-  uint64_t* o_done = p_full + NSB;       // [NSB]: O^T += V^T P^T(j) done
+  uint64_t* s_full = sc_full + NS;       // [NSB]: S^T(J) in buffer J % NSB
+  uint64_t* p_full = s_full + NSB;       // [NSB]: P^T(J) in shared buffer J % NSB
+  uint64_t* o_done = p_full + NSB;       // [NSB]: O^T += V^T P^T(J) done
   uint64_t* mx_full = o_done + NSB;      // [2]: the four warps' row maxima, exchange e in slot e % 2
-  uint64_t* fl_full = mx_full + 2;       // [2]: the four warps' flags of tile j >= 1 in slot (j - 1) % 2
-  uint64_t* q_ready = fl_full + 2;
-  uint64_t* app = q_ready + 1;
+  uint64_t* fl_full = mx_full + 2;       // [2]: the four warps' flags, exchange e in slot e % 2
+  uint64_t* q_ready = fl_full + 2;       // [2]: Q of piece i in buffer i % 2
+  uint64_t* seg_done = q_ready + 2;      // every MMA of a piece completed (one phase per piece)
+  uint64_t* o_free = seg_done + 1;       // the softmax warps have read a piece's O^T
+  uint64_t* app = o_free + 1;
   uint64_t* drain = app + 1;
-  uint64_t* fin = drain + 1;             // the four warps' row sums
+  uint64_t* fin = drain + 1;             // the four warps' row sums (one phase per piece)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   int* s_F = reinterpret_cast<int*>(tslot + 2);     // [8]
@@ -931,11 +961,13 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(&mx_full[0], 4);
-    mbar_init(&mx_full[1], 4);
-    mbar_init(&fl_full[0], 4);
-    mbar_init(&fl_full[1], 4);
-    mbar_init(q_ready, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&mx_full[i], 4);
+      mbar_init(&fl_full[i], 4);
+      mbar_init(&q_ready[i], 4);
+    }
+    mbar_init(seg_done, 1);
+    mbar_init(o_free, 4);
     mbar_init(app, NDW);
     mbar_init(drain, 1);
     mbar_init(fin, 4);
@@ -963,69 +995,61 @@ __global__ void __launch_bounds__(448, 1)
   tc::fence_after();
   const uint32_t tmem = *tslot;
 
-  // ---- the split plan of decode.cuh --------------------------------------------
+  // ---- the pieces of this CTA --------------------------------------------------
   int total = 0, maxp = 0;
   for (int bb = 0; bb < a.B; ++bb) {
     const int np = (s_F[bb] + 63) >> 6;
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
-  int b = -1, split = 0, nsplit = 0, npages = 0;
-  {
-    int acc = 0;
-    for (int bb = 0; bb < a.B; ++bb) {
-      const int np = (s_F[bb] + 63) >> 6;
-      const int ns = max(1, (np + chunk - 1) / chunk);
-      if (static_cast<int>(blockIdx.x) < acc + ns) {
-        b = bb;
-        split = blockIdx.x - acc;
-        nsplit = ns;
-        npages = np;
-        break;
-      }
-      acc += ns;
-    }
-  }
-  const int F = b >= 0 ? s_F[b] : 0;
-  const int p0 = split * chunk;
-  const int n = b >= 0 ? min(chunk, npages - p0) : 0;  // pages of this CTA
-  const int nt = (n + PPT - 1) / PPT;                  // key tiles
-  const int app_lo = early ? (F - a.T) >> 6 : 0x7fffffff;
+  const int chunk = max(split_chunk(total, a.nseg, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  int nsegs = 0;
+  for (int bb = 0; bb < a.B; ++bb) nsegs += max(1, (((s_F[bb] + 63) >> 6) + chunk - 1) / chunk);
+  const int s_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nsegs / gridDim.x);
+  const int s_hi = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * nsegs / gridDim.x);
   const int R_real = a.T * a.G;
-  const int32_t* trow = a.tables + static_cast<int64_t>(b >= 0 ? s_row[b] : 0) * a.L;
+  auto trow_of = [&](int bb) { return a.tables + static_cast<int64_t>(s_row[bb]) * a.L; };
 
-  if (b < 0) {
+  if (s_hi <= s_lo) {
     // no work: only the TMEM allocation is released below
   } else if (warp == 12) {
     // -------------------- TMA producer of raw code / scale pages --------------------
     if (lane == 0) {
-      bool app_seen = false;
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        int g = trow[p0 + i];
-        if (g < 0 || g >= a.M) {
-          set_status(a.status, NK_STATUS_PAGE_RANGE);
-          g = 0;
-        }
-        const int s = i % NR;
-        if (p0 + i >= app_lo && !app_seen) {  // this page receives new tokens: wait for them
-          app_seen = true;
-          if (!mbar_wait_bounded(app, 0, a.status)) { *s_abort = 1; break; }
-        }
-        if (i >= NR && !mbar_wait_bounded(&raw_empty[s], ((i / NR) - 1) & 1, a.status)) { *s_abort = 1; break; }
-        uint8_t* st = sRaw + s * Cfg::RAW;
-        const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
-        mbar_arrive_expect_tx(&raw_full[s], Cfg::TX);
+      bool app_seen = false, ok = true;
+      int issued = 0;  // pages of the CTA so far: the stage ring runs across pieces
+      for (int sg = s_lo; ok && sg < s_hi; ++sg) {
+        const VSeg g0 = vt_seg(sg, s_F, a.B, chunk);
+        const int32_t* trow = trow_of(g0.b);
+        const int app_lo = early ? (g0.F - a.T) >> 6 : 0x7fffffff;
+        for (int i = 0; i < g0.n; ++i) {
+          int g = trow[g0.p0 + i];
+          if (g < 0 || g >= a.M) {
+            set_status(a.status, NK_STATUS_PAGE_RANGE);
+            g = 0;
+          }
+          const int s = issued % NR;
+          if (g0.p0 + i >= app_lo && !app_seen) {  // this page receives new tokens: wait for them
+            app_seen = true;
+            if (!mbar_wait_bounded(app, 0, a.status)) { *s_abort = 1; ok = false; break; }
+          }
+          if (issued >= NR && !mbar_wait_bounded(&raw_empty[s], ((issued / NR) - 1) & 1, a.status)) {
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = sRaw + s * Cfg::RAW;
+          const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
+          mbar_arrive_expect_tx(&raw_full[s], Cfg::TX);
 #pragma unroll
-        for (int c = 0; c < Cfg::KCB / Cfg::K_RB; ++c)
-          tma_load_2d(st + c * 64 * Cfg::K_RB, &tmk, c * Cfg::K_RB, y, &raw_full[s]);
+          for (int c = 0; c < Cfg::KCB / Cfg::K_RB; ++c)
+            tma_load_2d(st + c * 64 * Cfg::K_RB, &tmk, c * Cfg::K_RB, y, &raw_full[s]);
 #pragma unroll
-        for (int c = 0; c < Cfg::VCB / Cfg::V_RB; ++c)
-          tma_load_2d(st + Cfg::R_KS + c * 64 * Cfg::V_RB, &tmv, c * Cfg::V_RB, y, &raw_full[s]);
-        bulk_load(st + Cfg::R_KSC, a.ks + static_cast<int64_t>(y) * Cfg::KSB, 64 * Cfg::KSB, &raw_full[s]);
-        bulk_load(st + Cfg::R_VSC, a.vs + static_cast<int64_t>(y) * Cfg::VSB, 64 * Cfg::VSB, &raw_full[s]);
-        ++issued;
+          for (int c = 0; c < Cfg::VCB / Cfg::V_RB; ++c)
+            tma_load_2d(st + Cfg::R_KS + c * 64 * Cfg::V_RB, &tmv, c * Cfg::V_RB, y, &raw_full[s]);
+          bulk_load(st + Cfg::R_KSC, a.ks + static_cast<int64_t>(y) * Cfg::KSB, 64 * Cfg::KSB, &raw_full[s]);
+          bulk_load(st + Cfg::R_VSC, a.vs + static_cast<int64_t>(y) * Cfg::VSB, 64 * Cfg::VSB, &raw_full[s]);
+          ++issued;
+        }
       }
       // after an abort, the copies still in flight land before the CTA exits
       for (int i = issued > NR ? issued - NR : 0; i < issued; ++i)
@@ -1033,49 +1057,70 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 13) {
     // ------------------------------ MMA issuer --------------------------------
-    // converged warp, lane 0 issues every MMA and commit (see vdecode_kernel)
-    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(q_ready, 0, a.status));
-    tc::fence_after();
+    // converged warp, lane 0 issues every MMA and commit (see vdecode_kernel).
+    // Tiles are numbered J across the CTA's pieces; within a piece the issue
+    // order is S^T(0), then S^T(j), O^T += V^T P^T(j - 1) for every tile j.
+    bool ok = true;
     const uint32_t v_base = smem_u32(sVf), p_base = smem_u32(sP);
-    const uint64_t qd = tc::smem_desc(smem_u32(sQ), 16, 1024);
-    // issue order S^T(0), then S^T(j), O^T += V^T P^T(j - 1) for every tile j
-    for (int j = 0; ok && j < nt + 1; ++j) {
-      if (j < nt) {
-        const int ks = j % NK, sb = j % NSB;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&kf_full[ks], (j / NK) & 1, a.status) && !*s_abort);
-        if (!ok) break;
-        tc::fence_after();
-        if (lane == 0) {
+    int J = 0;
+    for (int sg = s_lo; ok && sg < s_hi; ++sg) {
+      const int i = sg - s_lo;  // piece of this CTA
+      const int nt = (vt_seg(sg, s_F, a.B, chunk).n + PPT - 1) / PPT;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&q_ready[i & 1], (i >> 1) & 1, a.status) && !*s_abort);
+      if (!ok) break;
+      tc::fence_after();
+      const uint64_t qd = tc::smem_desc(smem_u32(sQ) + (i & 1) * Cfg::QB, 16, 1024);
+      // O^T of the previous piece must have been read before this piece's
+      // first O^T += V^T P^T overwrites it
+      bool o_waited = i == 0;
+      for (int j = 0; ok && j < nt + 1; ++j) {
+        if (j < nt) {
+          const int jg = J + j, ks = jg % NK, sb = jg % NSB;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&kf_full[ks], (jg / NK) & 1, a.status) && !*s_abort);
+          if (!ok) break;
+          tc::fence_after();
+          if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma_ts(tmem + Cfg::COL_S + 32 * sb, tmem + Cfg::COL_K + ks * (D / 2) + kk * 8,
-                       qd + static_cast<uint64_t>(((kk >> 2) * Cfg::QCHUNK + (kk & 3) * 32) >> 4), Cfg::ID_S,
-                       kk > 0);
-          tc::commit(&s_full[sb]);
-          tc::commit(&kf_empty[ks]);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc::mma_ts(tmem + Cfg::COL_S + 32 * sb, tmem + Cfg::COL_K + ks * (D / 2) + kk * 8,
+                         qd + static_cast<uint64_t>(((kk >> 2) * Cfg::QCHUNK + (kk & 3) * 32) >> 4), Cfg::ID_S,
+                         kk > 0);
+            tc::commit(&s_full[sb]);
+            tc::commit(&kf_empty[ks]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-      }
-      if (j >= 1) {
-        const int jj = j - 1, vs = jj % NV, pb = jj % NSB;
-        ok = mbar_wait_bounded(&vf_full[vs], (jj / NV) & 1, a.status) && !*s_abort;
-        if (ok) ok = mbar_wait_bounded(&p_full[pb], (jj / NSB) & 1, a.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc::fence_after();
-        const uint64_t vd = tc::smem_desc(v_base + vs * Cfg::F16V, Cfg::CHUNK, 1024);
-        const uint64_t pd = tc::smem_desc(p_base + pb * Cfg::PB, 16, 1024);
-        if (lane == 0) {
+        if (j >= 1) {
+          const int jj = j - 1, jg = J + jj, vs = jg % NV, pb = jg % NSB;
+          if (!o_waited) {
+            o_waited = true;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_free, (i - 1) & 1, a.status) && !*s_abort);
+            if (!ok) break;
+          }
+          ok = mbar_wait_bounded(&vf_full[vs], (jg / NV) & 1, a.status) && !*s_abort;
+          if (ok) ok = mbar_wait_bounded(&p_full[pb], (jg / NSB) & 1, a.status);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc::fence_after();
+          const uint64_t vd = tc::smem_desc(v_base + vs * Cfg::F16V, Cfg::CHUNK, 1024);
+          const uint64_t pd = tc::smem_desc(p_base + pb * Cfg::PB, 16, 1024);
+          if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk)
-            tc::mma_ss(tmem + Cfg::COL_O, vd + static_cast<uint64_t>((kk * 2048) >> 4),
-                       pd + static_cast<uint64_t>(((kk >> 2) * Cfg::PCHUNK + (kk & 3) * 32) >> 4), Cfg::ID_O,
-                       (jj > 0 || kk > 0));
-          tc::commit(&o_done[pb]);
-          tc::commit(&vf_empty[vs]);
+            for (int kk = 0; kk < TK / 16; ++kk)
+              tc::mma_ss(tmem + Cfg::COL_O, vd + static_cast<uint64_t>((kk * 2048) >> 4),
+                         pd + static_cast<uint64_t>(((kk >> 2) * Cfg::PCHUNK + (kk & 3) * 32) >> 4), Cfg::ID_O,
+                         (jj > 0 || kk > 0));
+            tc::commit(&o_done[pb]);
+            tc::commit(&vf_empty[vs]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
+      if (ok && !o_waited)  // a piece without pages still keeps the o_free phases in step
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_free, (i - 1) & 1, a.status) && !*s_abort);
+      if (lane == 0) tc::commit(seg_done);
+      __syncwarp();
+      J += nt;
     }
     if (lane == 0) {
       if (!ok) *s_abort = 1;
@@ -1097,114 +1142,129 @@ __global__ void __launch_bounds__(448, 1)
     if (early) {  // the new tokens whose pages this CTA reads, one warp per token
       constexpr int KCBW = code_row_bytes<KK>(D), VCBW = code_row_bytes<KV>(D);
       constexpr int KSBW = scale_row_bytes<KK>(D), VSBW = scale_row_bytes<KV>(D);
-      for (int t = dw; t < a.T; t += NDW) {
-        const int pos = F - a.T + t, pg = pos >> 6;
-        if (pg < p0 || pg >= p0 + n) continue;
-        const int g = trow[pg];
-        if (g < 0 || g >= a.M) {
-          if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
-          continue;
+      for (int sg = s_lo; sg < s_hi; ++sg) {
+        const VSeg g0 = vt_seg(sg, s_F, a.B, chunk);
+        const int32_t* trow = trow_of(g0.b);
+        for (int t = dw; t < a.T; t += NDW) {
+          const int pos = g0.F - a.T + t, pg = pos >> 6;
+          if (pg < g0.p0 || pg >= g0.p0 + g0.n) continue;
+          const int g = trow[pg];
+          if (g < 0 || g >= a.M) {
+            if (lane == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
+            continue;
+          }
+          const int64_t token_row = tile_row(g, h, a.H, a.M, a.head_major) + (pos & 63);
+          const int64_t src = ((static_cast<int64_t>(g0.b) * a.T + t) * a.H + h) * D;
+          encode_row<KK, D>(a.k_new + src, a.kc_w + token_row * KCBW, a.ks_w + token_row * KSBW, lane);
+          encode_row<KV, D>(a.v_new + src, a.vc_w + token_row * VCBW, a.vs_w + token_row * VSBW, lane);
         }
-        const int64_t token_row = tile_row(g, h, a.H, a.M, a.head_major) + (pos & 63);
-        const int64_t src = ((static_cast<int64_t>(b) * a.T + t) * a.H + h) * D;
-        encode_row<KK, D>(a.k_new + src, a.kc_w + token_row * KCBW, a.ks_w + token_row * KSBW, lane);
-        encode_row<KV, D>(a.v_new + src, a.vc_w + token_row * VCBW, a.vs_w + token_row * VSBW, lane);
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");
       __syncwarp();
       if (lane == 0) v_arrive(app);
     }
-    for (int j = 0; j < nt; ++j) {
-      const int npg = min(PPT, n - PPT * j);                // pages of this tile
-      const int kv_lim = min(F - 64 * (p0 + PPT * j), 64 * npg);  // keys of the tile below the frontier
-      bool ok = true;
-      const uint8_t* st[PPT];
+    bool ok = true;
+    int J = 0, ip = 0;  // tiles and pages of the CTA before this piece
+    for (int sg = s_lo; ok && sg < s_hi; ++sg) {
+      const VSeg g0 = vt_seg(sg, s_F, a.B, chunk);
+      const int n = g0.n, nt = (n + PPT - 1) / PPT;
+      for (int j = 0; j < nt; ++j) {
+        const int jg = J + j;
+        const int npg = min(PPT, n - PPT * j);                          // pages of this tile
+        const int kv_lim = min(g0.F - 64 * (g0.p0 + PPT * j), 64 * npg);  // keys of the tile below the frontier
+        const uint8_t* st[PPT];
 #pragma unroll
-      for (int pi = 0; pi < PPT; ++pi) {
-        const int i = PPT * j + min(pi, npg - 1);
-        st[pi] = sRaw + (i % NR) * Cfg::RAW;
-        if (pi < npg && ok) ok = mbar_wait_bounded(&raw_full[i % NR], (i / NR) & 1, a.status) && !*s_abort;
-      }
-      // the tile's key factors and value scales (slot reuse as in vdecode_kernel)
-      if (ok && dt < TK) {
-        float* sc = sSc + (j % NS) * 2 * TK;
-        const int pi = dt / 64, row = dt % 64;
-        const uint8_t* sp = sRaw + ((PPT * j + pi) % NR) * Cfg::RAW;  // read only when pi < npg
-        float kscale = 1.f, vscale = 1.f;
-        if (pi < npg) {
-          if constexpr (KK == KIND_FP8)
-            kscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_KSC + row * 2));
-          if constexpr (KV == KIND_FP8)
-            vscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_VSC + row * 2));
+        for (int pi = 0; pi < PPT; ++pi) {
+          const int ig = ip + PPT * j + min(pi, npg - 1);
+          st[pi] = sRaw + (ig % NR) * Cfg::RAW;
+          if (pi < npg && ok) ok = mbar_wait_bounded(&raw_full[ig % NR], (ig / NR) & 1, a.status) && !*s_abort;
         }
-        sc[dt] = kscale * a.softmax_scale * kLog2e;
-        sc[TK + dt] = dt < kv_lim ? vscale : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) v_arrive(&sc_full[j % NS]);
-      // K buffer j % NK: see the orderings of vdecode_kernel (same issue order)
-      static_assert(NS >= NV + 1 && NK == NV, "the waits these orderings rely on");
-      if (ok && j == NK) ok = mbar_wait_bounded(&kf_empty[0], 0, a.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok && kpg < npg) {  // keys of a missing page are masked in the softmax
-        uint32_t kw[D / 4];
-        const uint8_t* ks = kpg == 0 ? st[0] : st[1];  // no run-time index into st
-        key_half_f16<KK, D, Cfg::K_RB>(ks, ks + Cfg::R_KSC + krow * Cfg::KSB, krow, hd, kw);
-        if constexpr (D == 128) {
-          tc::st32(k_taddr + (j % NK) * (D / 2), kw);
-        } else {
-          tc::st16(k_taddr + (j % NK) * (D / 2), kw);
-        }
-        tc::wait_st();
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) v_arrive(&kf_full[j % NK]);
-      if (ok && j >= NV) ok = mbar_wait_bounded(&vf_empty[j % NV], ((j / NV) - 1) & 1, a.status);
-      if (ok) {
-        uint8_t* vt = sVf + (j % NV) * Cfg::F16V;
-        RawUnit ru[PPT * Cfg::PASSES];
-#pragma unroll
-        for (int pi = 0; pi < PPT; ++pi)
-#pragma unroll
-          for (int k = 0; k < Cfg::PASSES; ++k)
-            if (64 * pi + r0 + Cfg::RPT * k < kv_lim)
-              ru[pi * Cfg::PASSES + k] =
-                  ld_unit<KV>(st[pi] + Cfg::R_KS + v_src + Cfg::RPT * k * Cfg::V_RB,
-                              st[pi] + Cfg::R_VSC + (r0 + Cfg::RPT * k) * Cfg::VSB + pu / 2);
-#pragma unroll
-        for (int pi = 0; pi < PPT; ++pi)
-#pragma unroll
-          for (int k = 0; k < Cfg::PASSES; ++k) {
-            const int key = 64 * pi + r0 + Cfg::RPT * k;
-            cvt_unit<KV>(ru[pi * Cfg::PASSES + k], vt + v_dst + (64 * pi + Cfg::RPT * k) * 128, key >= kv_lim);
+        // the tile's key factors and value scales (slot reuse as in vdecode_kernel)
+        if (ok && dt < TK) {
+          float* sc = sSc + (jg % NS) * 2 * TK;
+          const int pi = dt / 64, row = dt % 64;
+          const uint8_t* sp = sRaw + ((ip + PPT * j + pi) % NR) * Cfg::RAW;  // read only when pi < npg
+          float kscale = 1.f, vscale = 1.f;
+          if (pi < npg) {
+            if constexpr (KK == KIND_FP8)
+              kscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_KSC + row * 2));
+            if constexpr (KV == KIND_FP8)
+              vscale = __half2float(*reinterpret_cast<const __half*>(sp + Cfg::R_VSC + row * 2));
           }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      __syncwarp();
-      if (lane == 0) v_arrive(&vf_full[j % NV]);
-      __syncwarp();
-      if (lane == 0) {
+          sc[dt] = kscale * a.softmax_scale * kLog2e;
+          sc[TK + dt] = dt < kv_lim ? vscale : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) v_arrive(&sc_full[jg % NS]);
+        // K buffer J % NK is free once S^T(J - NK) has completed.  (The scale
+        // slot J % NS is free as in vdecode_kernel: P V runs in order of J,
+        // across pieces too.)
+        static_assert(NS >= NV + 1, "the scale-slot ordering");
+        if (ok && jg >= NK) ok = mbar_wait_bounded(&kf_empty[jg % NK], ((jg / NK) - 1) & 1, a.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && kpg < npg) {  // keys of a missing page are masked in the softmax
+          uint32_t kw[D / 4];
+          const uint8_t* ks = kpg == 0 ? st[0] : st[1];  // no run-time index into st
+          key_half_f16<KK, D, Cfg::K_RB>(ks, ks + Cfg::R_KSC + krow * Cfg::KSB, krow, hd, kw);
+          if constexpr (D == 128) {
+            tc::st32(k_taddr + (jg % NK) * (D / 2), kw);
+          } else {
+            tc::st16(k_taddr + (jg % NK) * (D / 2), kw);
+          }
+          tc::wait_st();
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) v_arrive(&kf_full[jg % NK]);
+        if (ok && jg >= NV) ok = mbar_wait_bounded(&vf_empty[jg % NV], ((jg / NV) - 1) & 1, a.status);
+        if (ok) {
+          uint8_t* vt = sVf + (jg % NV) * Cfg::F16V;
+          RawUnit ru[PPT * Cfg::PASSES];
 #pragma unroll
-        for (int pi = 0; pi < PPT; ++pi)
-          if (pi < npg) v_arrive(&raw_empty[(PPT * j + pi) % NR]);
+          for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+            for (int k = 0; k < Cfg::PASSES; ++k)
+              if (64 * pi + r0 + Cfg::RPT * k < kv_lim)
+                ru[pi * Cfg::PASSES + k] =
+                    ld_unit<KV>(st[pi] + Cfg::R_KS + v_src + Cfg::RPT * k * Cfg::V_RB,
+                                st[pi] + Cfg::R_VSC + (r0 + Cfg::RPT * k) * Cfg::VSB + pu / 2);
+#pragma unroll
+          for (int pi = 0; pi < PPT; ++pi)
+#pragma unroll
+            for (int k = 0; k < Cfg::PASSES; ++k) {
+              const int key = 64 * pi + r0 + Cfg::RPT * k;
+              cvt_unit<KV>(ru[pi * Cfg::PASSES + k], vt + v_dst + (64 * pi + Cfg::RPT * k) * 128, key >= kv_lim);
+            }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) v_arrive(&vf_full[jg % NV]);
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int pi = 0; pi < PPT; ++pi)
+            if (pi < npg) v_arrive(&raw_empty[(ip + PPT * j + pi) % NR]);
+        }
+        if (!ok) {
+          *s_abort = 1;
+          break;
+        }
       }
-      if (!ok) {
-        *s_abort = 1;
-        break;
-      }
+      J += nt;
+      ip += n;
     }
   } else {
     // ---- softmax and output: warp w owns keys [32 w, 32 w + 32) of every tile ----
     const int kq = 32 * warp + lane;  // this thread's key in a tile
     const uint32_t lq = static_cast<uint32_t>(32 * warp) << 16;
     if (early) griddep_wait();
-    // Q: one power-of-two scale 2^e for all the CTA's query rows; this warp
-    // writes rows [8 w, 8 w + 8) of the K-major B operand
-    float rs;
-    {
+    // Q of piece sg into buffer qb: one power-of-two scale 2^e for its query
+    // rows (returned: 2^-e); this warp writes rows [8 w, 8 w + 8) of the
+    // K-major B operand
+    auto write_q = [&](int sg, int qb) -> float {
+      const int bq = vt_seg(sg, s_F, a.B, chunk).b;
       auto qrow = [&](int r) {
-        return a.q + ((static_cast<int64_t>(b) * a.T + r / a.G) * a.Hq + h * a.G + r % a.G) * D;
+        return a.q + ((static_cast<int64_t>(bq) * a.T + r / a.G) * a.Hq + h * a.G + r % a.G) * D;
       };
       float mx = 0.f;
       for (int u = lane; u < R_real * (D / 8); u += 32) {
@@ -1219,7 +1279,7 @@ __global__ void __launch_bounds__(448, 1)
       if (mx > 0.f) frexpf(mx, &ex);
       const int e = mx > 0.f ? min(15 - ex, 100) : 0;  // 2^e stays finite in fp32
       const float qf = ldexpf(1.f, e);
-      rs = ldexpf(1.f, -e);
+      uint8_t* qbuf = sQ + qb * Cfg::QB;
       for (int u = lane; u < 8 * (D / 8); u += 32) {
         const int r = 8 * warp + u / (D / 8), c = u % (D / 8);
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
@@ -1231,216 +1291,239 @@ __global__ void __launch_bounds__(448, 1)
           const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
           o[k] = pack_f16x2(__low2float(v) * qf, __high2float(v) * qf);
         }
-        *reinterpret_cast<uint4*>(sQ + (c / 8) * Cfg::QCHUNK + swz<128>(r, (c % 8) * 16)) =
+        *reinterpret_cast<uint4*>(qbuf + (c / 8) * Cfg::QCHUNK + swz<128>(r, (c % 8) * 16)) =
             make_uint4(o[0], o[1], o[2], o[3]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) v_arrive(q_ready);
-    }
+      if (lane == 0) v_arrive(&q_ready[qb]);
+      return ldexpf(1.f, -e);
+    };
+    float rs_cur = write_q(s_lo, 0);
+    float rs_next = s_lo + 1 < s_hi ? write_q(s_lo + 1, 1) : 1.f;
     // P^T (K-major, 32 query rows x TK keys): element (row r, key kq)
     const uint32_t p_col = smem_u32(sP) + (kq / 64) * Cfg::PCHUNK;
     const int p_byte = (kq % 64) * 2;
     // -(running maximum of row r), 0 while it is -inf: this warp's copy, written by lane r
     float* mn = sMn + 32 * warp;
-    mn[lane] = 0.f;
-    __syncwarp();
-    float lacc[32];  // row sums of this thread's key
-#pragma unroll
-    for (int r = 0; r < 32; ++r) lacc[r] = 0.f;
-    float m_self = -INFINITY;        // the running maximum of row `lane`
-    uint32_t inf_rows = 0xffffffffu;  // rows whose running maximum is still -inf
-    int nfull = 0;                    // exchanges of row maxima so far
+    int nfull = 0, nflag = 0;  // exchanges of row maxima and of flags so far
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int sb = j % NSB, ss = j % NS;
-      ok = mbar_wait_bounded(&s_full[sb], (j / NSB) & 1, a.status) && !*s_abort;
-      if (ok) ok = mbar_wait_bounded(&sc_full[ss], (j / NS) & 1, a.status) && !*s_abort;
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        *s_abort = 1;
-        break;
-      }
-      tc::fence_after();
-      // t[r] = z - m of row r for this key: z = s * key factor * 2^-e, m the
-      // running maximum (0 while -inf); -inf where the key is masked
-      float t[32];
-      {
-        uint32_t v[32];
-        tc::ld32(tmem + lq + Cfg::COL_S + 32 * sb, v);
-        tc::wait_ld();
-        const float kfr = sSc[ss * 2 * TK + kq] * rs;
-        const int kt0 = 64 * (p0 + PPT * j);
-        const int key_end = 64 * (p0 + min(PPT * j + PPT, n));  // keys of this CTA in the tile end here
-        const bool all_vis = kt0 + TK - 1 <= F - a.T && kt0 + TK <= key_end;  // every key visible to every row
-        const int key = kt0 + kq, d = key - (F - a.T);
-        // key k is visible to rows r with r / G >= k - (F - T)
-        const int rmin = all_vis ? 0 : (key >= key_end ? 32 : (d <= 0 ? 0 : min(32, a.G * d)));
+    int J = 0;
+    for (int sg = s_lo; ok && sg < s_hi; ++sg) {
+      const int i = sg - s_lo;
+      const VSeg g0 = vt_seg(sg, s_F, a.B, chunk);
+      const int n = g0.n, nt = (n + PPT - 1) / PPT, F = g0.F, p0 = g0.p0;
+      const float rs = rs_cur;
+      mn[lane] = 0.f;
+      __syncwarp();
+      float lacc[32];  // row sums of this thread's key
 #pragma unroll
-        for (int r4 = 0; r4 < 32; r4 += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(mn + r4);
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            t[r4 + i] = r4 + i >= rmin ? fmaf(__uint_as_float(v[r4 + i]), kfr, mm[i]) : -INFINITY;
-        }
-      }
-      // Does a row's maximum move past the lazy threshold (or leave -inf)?
-      // The first tile always sets the maxima; later tiles exchange one flag
-      // per warp and take the exact per-row reduction only when one is set.
-      bool full = j == 0;
-      if (!full) {
-        float tm = t[0];
-#pragma unroll
-        for (int r = 1; r < 32; ++r) tm = fmaxf(tm, t[r]);
-        bool fl = tm > Cfg::THR;
-        if (inf_rows != 0u) {
-#pragma unroll
-          for (int r = 0; r < 32; ++r) fl |= ((inf_rows >> r) & 1u) && t[r] > -INFINITY;
-        }
-        fl = __any_sync(0xffffffffu, fl);
-        const int e = j - 1;
-        int* fls = sFl + (e & 1) * 4;
-        if (lane == 0) {
-          fls[warp] = fl ? 1 : 0;
-          v_arrive(&fl_full[e & 1]);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&fl_full[e & 1], (e >> 1) & 1, a.status) && !*s_abort)) {
-          ok = false;
-          *s_abort = 1;
-          break;
-        }
-        const int4 f4 = *reinterpret_cast<const int4*>(fls);
-        full = (f4.x | f4.y | f4.z | f4.w) != 0;
-      }
-      bool moved = false;
-      float fac = 1.f;
-      if (full) {
-        // exact row maxima: this warp's over lanes, then the four warps' through shared memory
-        float* mx = sMx + (nfull & 1) * 128;
-        mx[32 * warp + lane] = xreduce32<true>(t, lane);
-        __syncwarp();
-        if (lane == 0) v_arrive(&mx_full[nfull & 1]);
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_bounded(&mx_full[nfull & 1], (nfull >> 1) & 1, a.status) && !*s_abort)) {
-          ok = false;
-          *s_abort = 1;
-          break;
-        }
-        const float gm = fmaxf(fmaxf(mx[lane], mx[32 + lane]), fmaxf(mx[64 + lane], mx[96 + lane]));
-        ++nfull;
-        const float mcur = m_self == -INFINITY ? 0.f : m_self;  // the value t is relative to
-        const float mnew = fmaxf(m_self, gm + mcur);
-        const bool resc = mnew != -INFINITY && (m_self == -INFINITY || mnew > m_self + Cfg::THR);
-        if (resc) {
-          fac = m_self == -INFINITY ? 0.f : ex2(m_self - mnew);
-          m_self = mnew;
-        }
-        const float mneg_new = m_self == -INFINITY ? 0.f : -m_self;
-        const float delta = mneg_new + mcur;  // t of row `lane` moves by this
-        mn[lane] = mneg_new;
-        inf_rows = __ballot_sync(0xffffffffu, m_self == -INFINITY);
-        moved = __any_sync(0xffffffffu, resc);
-        if (moved) {
-#pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            lacc[r] *= __shfl_sync(0xffffffffu, fac, r);
-            t[r] += __shfl_sync(0xffffffffu, delta, r);
-          }
-        }
-        __syncwarp();
-      }
-      // P = 2^t, stored as f16 into column kq of the K-major P^T tile
-      const uint32_t pb = p_col + sb * Cfg::PB;
-      float vsc = 1.f;
-      if constexpr (KV == KIND_FP8) vsc = sSc[ss * 2 * TK + TK + kq];
-#pragma unroll
-      for (int r = 0; r < 32; r += 2) {
-        const float p0v = ex2(t[r]), p1v = ex2(t[r + 1]);
-        lacc[r] += p0v;
-        lacc[r + 1] += p1v;
-        const uint32_t w = KV == KIND_FP8 ? pack_f16x2(p0v * vsc, p1v * vsc) : pack_f16x2(p0v, p1v);
-        st_shared_u16(pb + swz<128>(r, p_byte), static_cast<uint16_t>(w & 0xFFFFu));
-        st_shared_u16(pb + swz<128>(r + 1, p_byte), static_cast<uint16_t>(w >> 16));
-      }
-      if (moved && j >= 1) {
-        // O^T is rescaled only when a row's maximum moved: O^T += V^T P^T(j - 1)
-        // must have landed first (the one before it has, as S^T(j) has completed);
-        // O^T += V^T P^T(j) waits for this warp's P^T
-        const int jp = j - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[jp % NSB], (jp / NSB) & 1, a.status) && !*s_abort)) {
+      for (int r = 0; r < 32; ++r) lacc[r] = 0.f;
+      float m_self = -INFINITY;        // the running maximum of row `lane`
+      uint32_t inf_rows = 0xffffffffu;  // rows whose running maximum is still -inf
+      for (int j = 0; j < nt; ++j) {
+        const int jg = J + j, sb = jg % NSB, ss = jg % NS;
+        ok = mbar_wait_bounded(&s_full[sb], (jg / NSB) & 1, a.status) && !*s_abort;
+        if (ok) ok = mbar_wait_bounded(&sc_full[ss], (jg / NS) & 1, a.status) && !*s_abort;
+        if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           *s_abort = 1;
           break;
         }
         tc::fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-          uint32_t ov[16];
-          tc::ld16(tmem + lq + Cfg::COL_O + c0, ov);
+        // t[r] = z - m of row r for this key: z = s * key factor * 2^-e, m the
+        // running maximum (0 while -inf); -inf where the key is masked
+        float t[32];
+        {
+          uint32_t v[32];
+          tc::ld32(tmem + lq + Cfg::COL_S + 32 * sb, v);
           tc::wait_ld();
+          const float kfr = sSc[ss * 2 * TK + kq] * rs;
+          const int kt0 = 64 * (p0 + PPT * j);
+          const int key_end = 64 * (p0 + min(PPT * j + PPT, n));  // keys of this piece in the tile end here
+          const bool all_vis = kt0 + TK - 1 <= F - a.T && kt0 + TK <= key_end;  // every key visible to every row
+          const int key = kt0 + kq, d = key - (F - a.T);
+          // key k is visible to rows r with r / G >= k - (F - T)
+          const int rmin = all_vis ? 0 : (key >= key_end ? 32 : (d <= 0 ? 0 : min(32, a.G * d)));
 #pragma unroll
-          for (int r = 0; r < 16; ++r)
-            ov[r] = __float_as_uint(__uint_as_float(ov[r]) * __shfl_sync(0xffffffffu, fac, c0 + r));
-          tc::st16(tmem + lq + Cfg::COL_O + c0, ov);
+          for (int r4 = 0; r4 < 32; r4 += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mn + r4);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              t[r4 + q4] = r4 + q4 >= rmin ? fmaf(__uint_as_float(v[r4 + q4]), kfr, mm[q4]) : -INFINITY;
+          }
         }
-        tc::wait_st();
+        // Does a row's maximum move past the lazy threshold (or leave -inf)?
+        // A piece's first tile always sets the maxima; later tiles exchange
+        // one flag per warp and take the exact per-row reduction only when one
+        // is set.
+        bool full = j == 0;
+        if (!full) {
+          float tm = t[0];
+#pragma unroll
+          for (int r = 1; r < 32; ++r) tm = fmaxf(tm, t[r]);
+          bool fl = tm > Cfg::THR;
+          if (inf_rows != 0u) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) fl |= ((inf_rows >> r) & 1u) && t[r] > -INFINITY;
+          }
+          fl = __any_sync(0xffffffffu, fl);
+          const int e = nflag++;
+          int* fls = sFl + (e & 1) * 4;
+          if (lane == 0) {
+            fls[warp] = fl ? 1 : 0;
+            v_arrive(&fl_full[e & 1]);
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&fl_full[e & 1], (e >> 1) & 1, a.status) && !*s_abort)) {
+            ok = false;
+            *s_abort = 1;
+            break;
+          }
+          const int4 f4 = *reinterpret_cast<const int4*>(fls);
+          full = (f4.x | f4.y | f4.z | f4.w) != 0;
+        }
+        bool moved = false;
+        float fac = 1.f;
+        if (full) {
+          // exact row maxima: this warp's over lanes, then the four warps' through shared memory
+          float* mx = sMx + (nfull & 1) * 128;
+          mx[32 * warp + lane] = xreduce32<true>(t, lane);
+          __syncwarp();
+          if (lane == 0) v_arrive(&mx_full[nfull & 1]);
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_bounded(&mx_full[nfull & 1], (nfull >> 1) & 1, a.status) && !*s_abort)) {
+            ok = false;
+            *s_abort = 1;
+            break;
+          }
+          const float gm = fmaxf(fmaxf(mx[lane], mx[32 + lane]), fmaxf(mx[64 + lane], mx[96 + lane]));
+          ++nfull;
+          const float mcur = m_self == -INFINITY ? 0.f : m_self;  // the value t is relative to
+          const float mnew = fmaxf(m_self, gm + mcur);
+          const bool resc = mnew != -INFINITY && (m_self == -INFINITY || mnew > m_self + Cfg::THR);
+          if (resc) {
+            fac = m_self == -INFINITY ? 0.f : ex2(m_self - mnew);
+            m_self = mnew;
+          }
+          const float mneg_new = m_self == -INFINITY ? 0.f : -m_self;
+          const float delta = mneg_new + mcur;  // t of row `lane` moves by this
+          mn[lane] = mneg_new;
+          inf_rows = __ballot_sync(0xffffffffu, m_self == -INFINITY);
+          moved = __any_sync(0xffffffffu, resc);
+          if (moved) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+              lacc[r] *= __shfl_sync(0xffffffffu, fac, r);
+              t[r] += __shfl_sync(0xffffffffu, delta, r);
+            }
+          }
+          __syncwarp();
+        }
+        // P = 2^t, stored as f16 into column kq of the K-major P^T tile
+        const uint32_t pb = p_col + sb * Cfg::PB;
+        float vsc = 1.f;
+        if constexpr (KV == KIND_FP8) vsc = sSc[ss * 2 * TK + TK + kq];
+#pragma unroll
+        for (int r = 0; r < 32; r += 2) {
+          const float p0v = ex2(t[r]), p1v = ex2(t[r + 1]);
+          lacc[r] += p0v;
+          lacc[r + 1] += p1v;
+          const uint32_t w = KV == KIND_FP8 ? pack_f16x2(p0v * vsc, p1v * vsc) : pack_f16x2(p0v, p1v);
+          st_shared_u16(pb + swz<128>(r, p_byte), static_cast<uint16_t>(w & 0xFFFFu));
+          st_shared_u16(pb + swz<128>(r + 1, p_byte), static_cast<uint16_t>(w >> 16));
+        }
+        if (moved && j >= 1) {
+          // O^T is rescaled only when a row's maximum moved: O^T += V^T P^T(J - 1)
+          // must have landed first (the one before it has, as S^T(J) has completed);
+          // O^T += V^T P^T(J) waits for this warp's P^T
+          const int jp = jg - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[jp % NSB], (jp / NSB) & 1, a.status) && !*s_abort)) {
+            ok = false;
+            *s_abort = 1;
+            break;
+          }
+          tc::fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < 32; c0 += 16) {
+            uint32_t ov[16];
+            tc::ld16(tmem + lq + Cfg::COL_O + c0, ov);
+            tc::wait_ld();
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+              ov[r] = __float_as_uint(__uint_as_float(ov[r]) * __shfl_sync(0xffffffffu, fac, c0 + r));
+            tc::st16(tmem + lq + Cfg::COL_O + c0, ov);
+          }
+          tc::wait_st();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) v_arrive(&p_full[sb]);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc::fence_before();
+      if (!ok) break;
+      // the piece's result: every MMA of it has completed once seg_done has
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(seg_done, i & 1, a.status) && !*s_abort);
+      tc::fence_after();
+      sL[32 * warp + lane] = xreduce32<false>(lacc, lane);
       __syncwarp();
-      if (lane == 0) v_arrive(&p_full[sb]);
-    }
-    // every MMA of the CTA has completed once drain has (committed after the last P V)
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(drain, 0, a.status) && !*s_abort);
-    tc::fence_after();
-    sL[32 * warp + lane] = xreduce32<false>(lacc, lane);
-    __syncwarp();
-    if (lane == 0) v_arrive(fin);
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(fin, 0, a.status) && !*s_abort);
-    if (ok) {
-      const float lt = (sL[lane] + sL[32 + lane]) + (sL[64 + lane] + sL[96 + lane]);  // row `lane`
-      const bool final_out = nsplit == 1;
-      const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + split;
-      const float inv_self = lt > 0.f ? 1.f / lt : 0.f;
-      const int dim = 32 * warp + lane;  // O^T lane: the dimension this thread writes
-      uint32_t ov[32];
-      if (n > 0) {
-        tc::ld32(tmem + lq + Cfg::COL_O, ov);
-        tc::wait_ld();
-      } else {
+      if (lane == 0) v_arrive(fin);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(fin, i & 1, a.status) && !*s_abort);
+      if (!ok) break;
+      {
+        const float lt = (sL[lane] + sL[32 + lane]) + (sL[64 + lane] + sL[96 + lane]);  // row `lane`
+        const int b = g0.b;
+        const bool final_out = g0.ns == 1;
+        const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + g0.k;
+        const float inv_self = lt > 0.f ? 1.f / lt : 0.f;
+        const int dim = 32 * warp + lane;  // O^T lane: the dimension this thread writes
+        uint32_t ov[32];
+        if (n > 0) {
+          tc::ld32(tmem + lq + Cfg::COL_O, ov);
+          tc::wait_ld();
+        } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) ov[r] = 0u;
-      }
-      if (32 * warp < D) {  // at D = 64 the lanes of quadrants 2 and 3 hold no dimension
+          for (int r = 0; r < 32; ++r) ov[r] = 0u;
+        }
+        // O^T and sL are read: the next piece may overwrite both
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) v_arrive(o_free);
+        if (32 * warp < D) {  // at D = 64 the lanes of quadrants 2 and 3 hold no dimension
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const float inv = __shfl_sync(0xffffffffu, inv_self, r);
-          if (r < R_real) {
-            const int ot = r / a.G, og = r % a.G;
-            if (final_out) {
-              a.out[((static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og) * D + dim] =
-                  __float2bfloat16_rn(__uint_as_float(ov[r]) * inv);
-            } else {
-              a.ws_acc[(part * R + r) * D + dim] = __uint_as_float(ov[r]);
+          for (int r = 0; r < 32; ++r) {
+            const float inv = __shfl_sync(0xffffffffu, inv_self, r);
+            if (r < R_real) {
+              const int ot = r / a.G, og = r % a.G;
+              if (final_out) {
+                a.out[((static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og) * D + dim] =
+                    __float2bfloat16_rn(__uint_as_float(ov[r]) * inv);
+              } else {
+                a.ws_acc[(part * R + r) * D + dim] = __uint_as_float(ov[r]);
+              }
             }
           }
         }
-      }
-      if (warp == 0 && lane < R_real) {
-        const int ot = lane / a.G, og = lane % a.G;
-        if (final_out) {
-          if (a.lse)
-            a.lse[(static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og] =
-                lt > 0.f ? (m_self + log2f(lt)) * kLn2 : -INFINITY;
-        } else {
-          a.ws_ml[part * R + lane] = make_float2(n > 0 ? m_self : -INFINITY, n > 0 ? lt : 0.f);
+        if (warp == 0 && lane < R_real) {
+          const int ot = lane / a.G, og = lane % a.G;
+          if (final_out) {
+            if (a.lse)
+              a.lse[(static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og] =
+                  lt > 0.f ? (m_self + log2f(lt)) * kLn2 : -INFINITY;
+          } else {
+            a.ws_ml[part * R + lane] = make_float2(n > 0 ? m_self : -INFINITY, n > 0 ? lt : 0.f);
+          }
         }
       }
+      J += nt;
+      // Q buffer i % 2 is free (every S^T of this piece has completed): the
+      // Q of piece i + 2 goes there
+      rs_cur = rs_next;
+      if (sg + 2 < s_hi) rs_next = write_q(sg + 2, i & 1);
     }
   }
 
-  if (warp == 0 && lane == 0 && b >= 0) mbar_wait_bounded(drain, 0, a.status, 200000000ull);
+  if (warp == 0 && lane == 0 && s_hi > s_lo) mbar_wait_bounded(drain, 0, a.status, 200000000ull);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
