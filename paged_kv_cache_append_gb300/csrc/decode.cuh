@@ -163,6 +163,13 @@ __host__ __device__ __forceinline__ int split_chunk(int total, int target, int B
   return c < 1 ? 1 : c;
 }
 
+// Pages per piece when a CTA takes several pieces (a budget of nseg pieces
+// per head): the pieces need not fit one wave, only each row's own slots.
+__host__ __device__ __forceinline__ int seg_chunk(int total, int nseg) {
+  const int c = (total + nseg - 1) / nseg;
+  return c < 1 ? 1 : c;
+}
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -900,7 +907,8 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(split_chunk(total, a.nseg > 0 ? a.nseg : a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = max(a.nseg > 0 ? seg_chunk(total, a.nseg) : split_chunk(total, a.target, a.B),
+                        (maxp + kMaxSplits - 1) / kMaxSplits);
   const int nsplit = max(1, (((s_F[b] + 63) >> 6) + chunk - 1) / chunk);
   griddep_wait();
   griddep_launch_dependents();
