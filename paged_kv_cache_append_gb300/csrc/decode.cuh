@@ -163,6 +163,25 @@ __host__ __device__ __forceinline__ int split_chunk(int total, int target, int B
   return c < 1 ? 1 : c;
 }
 
+// The smallest chunk (at least ceil(maxp / kMaxSplits)) whose splits,
+// max(1, ceil(N_b / chunk)) for every row, add up to at most `target`:
+// split_chunk's value always qualifies, a bisection finds the least one, so
+// the longest split is as short as one wave allows.
+__device__ __forceinline__ int wave_chunk(const int* s_F, int B, int total, int maxp, int target) {
+  const int floor_c = (maxp + kMaxSplits - 1) / kMaxSplits;
+  int hi = max(split_chunk(total, target, B), floor_c);
+  int lo = max(max(1, floor_c), (total + target - 1) / max(target, 1));
+  if (lo > hi) lo = hi;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    int n = 0;
+    for (int bb = 0; bb < B; ++bb) n += max(1, (((s_F[bb] + 63) >> 6) + mid - 1) / mid);
+    if (n <= target) hi = mid;
+    else lo = mid + 1;
+  }
+  return hi;
+}
+
 // Pages per piece when a CTA takes several pieces (a budget of nseg pieces
 // per head): the pieces need not fit one wave, only each row's own slots.
 __host__ __device__ __forceinline__ int seg_chunk(int total, int nseg) {
@@ -258,7 +277,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = wave_chunk(s_F, a.B, total, maxp, a.target);
   int b = -1, split = 0, nsplit = 0, npages = 0;
   {
     int acc = 0;
@@ -907,8 +926,8 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(a.nseg > 0 ? seg_chunk(total, a.nseg) : split_chunk(total, a.target, a.B),
-                        (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = a.nseg > 0 ? max(seg_chunk(total, a.nseg), (maxp + kMaxSplits - 1) / kMaxSplits)
+                                : wave_chunk(s_F, a.B, total, maxp, a.target);
   const int nsplit = max(1, (((s_F[b] + 63) >> 6) + chunk - 1) / chunk);
   griddep_wait();
   griddep_launch_dependents();

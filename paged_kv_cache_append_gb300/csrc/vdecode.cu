@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(448, 1)
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(split_chunk(total, a.target, a.B), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = wave_chunk(s_F, a.B, total, maxp, a.target);
   int b = -1, split = 0, nsplit = 0, npages = 0;
   {
     int acc = 0;
