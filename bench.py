@@ -58,7 +58,8 @@ def peaks_tensor():
 def traffic(workload, kernel, algorithmic_now):
     """DRAM bytes per launch of the roofline kernel from the committed ncu
     capture (profiles/traffic.json), scaled by algorithmic work to this
-    launch; None when the kernel's sources changed since the capture."""
+    launch (all but its fixed part); None when the kernel's sources changed
+    since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -77,7 +78,9 @@ def traffic(workload, kernel, algorithmic_now):
             return None
     if h.hexdigest() != ent["sha256"]:
         return None
-    return int(round(ent["dram_bytes_per_launch"] * algorithmic_now / ent["algorithmic_per_launch_at_capture"]))
+    fixed = ent.get("fixed_bytes_per_launch", 0)  # bytes that do not grow with the work (split partials)
+    return int(round((ent["dram_bytes_per_launch"] - fixed) * algorithmic_now
+                     / ent["algorithmic_per_launch_at_capture"] + fixed))
 
 
 def make_workload(name, layers=None, context=None):
