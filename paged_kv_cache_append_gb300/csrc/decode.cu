@@ -126,6 +126,7 @@ static int run_decode(const void* q, int32_t Hq, const nk_pool* pool, int32_t la
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
   a.nseg = pl.nseg;
+  a.ctas = pl.ctas;
   a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   if (k_new) {
     a.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -227,6 +228,7 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
   a.C = pool->desc.max_concurrency;
   a.target = pl.target;
   a.nseg = pl.nseg;
+  a.ctas = pl.ctas;
   a.head_major = pool->desc.order == NK_HEAD_MAJOR;
   cudaError_t e = pl.fn(pool, layer, a, pl.nqt, dim3(pl.ctas, a.H), s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

@@ -73,6 +73,7 @@ struct DecodeArgs {
   int target;    // partial slots per (row, KV head) (= maxsplit); with nseg == 0 also the
                  // splits per head the chunking aims at, one CTA each
   int nseg = 0;  // > 0: pieces per head the chunking aims at, several per CTA (vdecode.cu)
+  int ctas = 0;  // CTAs per KV head of the decode launch (read when nseg > 0)
   int head_major = 0;  // plane order
 };
 
@@ -187,6 +188,16 @@ __device__ __forceinline__ int wave_chunk(const int* s_F, int B, int total, int 
 __host__ __device__ __forceinline__ int seg_chunk(int total, int nseg) {
   const int c = (total + nseg - 1) / nseg;
   return c < 1 ? 1 : c;
+}
+
+// Pages per piece of the kernel that takes several pieces per CTA: about
+// total / nseg while that leaves pieces of at least 64 pages; shorter pieces
+// would cost more in per-piece hand-offs than they win in balance, so the
+// plan falls back to one wave-filling split per CTA.
+__device__ __forceinline__ int piece_chunk(const int* s_F, const DecodeArgs& a, int total, int maxp) {
+  const int c = seg_chunk(total, a.nseg);
+  if (c >= 64) return max(c, (maxp + kMaxSplits - 1) / kMaxSplits);
+  return wave_chunk(s_F, a.B, total, maxp, min(a.ctas, a.target));
 }
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
@@ -926,8 +937,7 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = a.nseg > 0 ? max(seg_chunk(total, a.nseg), (maxp + kMaxSplits - 1) / kMaxSplits)
-                                : wave_chunk(s_F, a.B, total, maxp, a.target);
+  const int chunk = a.nseg > 0 ? piece_chunk(s_F, a, total, maxp) : wave_chunk(s_F, a.B, total, maxp, a.target);
   const int nsplit = max(1, (((s_F[b] + 63) >> 6) + chunk - 1) / chunk);
   griddep_wait();
   griddep_launch_dependents();

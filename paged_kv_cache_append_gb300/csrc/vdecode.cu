@@ -871,9 +871,10 @@ __device__ __forceinline__ void key_half_f16(const uint8_t* stage, const uint8_t
 }
 
 // One piece of a head's work: pages [p0, p0 + n) of row b, piece k of ns.
-// A head's rows are cut in row order into pieces of `chunk` pages (about
-// total / a.nseg, at most kMaxSplits pieces a row); CTA x of gridDim.x takes
-// pieces [x S / gridDim.x, (x + 1) S / gridDim.x) of the S pieces.
+// A head's rows are cut in row order into pieces of `chunk` pages
+// (piece_chunk: about total / a.nseg, or one wave-filling split per CTA when
+// that would make pieces short); CTA x of gridDim.x takes pieces
+// [x S / gridDim.x, (x + 1) S / gridDim.x) of the S pieces.
 struct VSeg {
   int b, k, ns, p0, n, F;
 };
@@ -1002,7 +1003,7 @@ __global__ void __launch_bounds__(448, 1)
     total += np;
     maxp = max(maxp, np);
   }
-  const int chunk = max(seg_chunk(total, a.nseg), (maxp + kMaxSplits - 1) / kMaxSplits);
+  const int chunk = piece_chunk(s_F, a, total, maxp);
   int nsegs = 0;
   for (int bb = 0; bb < a.B; ++bb) nsegs += max(1, (((s_F[bb] + 63) >> 6) + chunk - 1) / chunk);
   const int s_lo = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nsegs / gridDim.x);
