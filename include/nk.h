@@ -207,6 +207,9 @@ int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t
  * kernel for every profile; 17 <= R <= 32 over FP8-row, NVFP4-G16 and K8V4
  * pools runs a 5th-generation tensor-core kernel (csrc/vdecode.cu), and over
  * BF16 and INT8-G64 pools the warp-level kernel at head_dim 64 and 128.
+ * The split count per (row, KV head) is at most 32; at head_dim 64 and 128
+ * the tensor-core kernel may take several splits per CTA.  Either way the
+ * partials fit the workspace that nk_decode_workspace_bytes reports.
  * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T < 1),
  * NK_ERR_UNSUPPORTED (R > 32, or R > 16 at head_dim 256 over BF16 or
  * INT8-G64 pools), NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
