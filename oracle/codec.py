@@ -11,11 +11,13 @@ quotient rounded once.
 BF16        codes are the bf16 bits, stored unchanged (no fp16 conversion on
             write, as the page requires for the BF16 profile).
 INT8-G64    per group of 64 elements along d:
-              amax = max|x|;  s = fp16(fp32(amax / 127))  (fp32 quotient,
-              then binary16 RNE);  q = clamp(RNE(x / s), -127, 127);
+              amax = max|x|;  s = min(fp16(fp32(amax / 127)), 65504)  (fp32
+              quotient, then binary16 RNE, saturating at the largest finite
+              binary16);  q = clamp(RNE(x / s), -127, 127);
               s == 0 gives q = 0.  Scale plane: binary16 bits.
 FP8-row     one scale per (token, head) row of D elements:
-              s = fp16(fp32(amax / 448));  c = E4M3FN_RNE_satfinite(x / s);
+              s = min(fp16(fp32(amax / 448)), 65504);
+              c = E4M3FN_RNE_satfinite(x / s);
               s == 0 gives c = 0x00.  Scale plane: binary16 bits.
 NVFP4-G16   per group of 16 elements along d:
               s8 = E4M3FN_RNE_satfinite(fp32(amax / 6))  (an E4M3 byte);
@@ -23,6 +25,10 @@ NVFP4-G16   per group of 16 elements along d:
               element 2i goes to the low nibble, 2i+1 to the high nibble of
               byte i.  No per-tensor global scale.
 K8V4        K uses FP8-row, V uses NVFP4-G16 (closed asymmetric profile).
+
+The binary16 scales saturate (a reading: the page fixes no overflow rule,
+and the E4M3 / E2M1 codes saturate too): without it a group with amax above
+127 * 65504 (or 448 * 65504) would store s = +inf and dequantize to NaN.
 
 A code's sign bit is the sign of the quotient, so -0.0 and negative values
 that round to zero encode as 0x80 (E4M3) or 0x8 (E2M1).  INT8 has no -0.
@@ -57,7 +63,7 @@ def int8_g64_quant(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     D = x.shape[-1]
     g = x.reshape(*x.shape[:-1], D // 64, 64)
     amax = np.max(np.abs(g), axis=-1)
-    s = F.round_fp16(_fp32_div(amax, 127.0))
+    s = np.minimum(F.round_fp16(_fp32_div(amax, 127.0)), F.FP16_MAX)
     with np.errstate(divide="ignore", invalid="ignore"):
         q = np.rint(g / s[..., None])
     q = np.where(s[..., None] == 0, 0.0, np.clip(q, -127, 127))
@@ -76,7 +82,7 @@ def int8_g64_dequant(codes: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
 def fp8_row_quant(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     """x [..., D] -> (E4M3 codes uint8 [..., D], scale bits uint16 [..., 1])."""
     amax = np.max(np.abs(x), axis=-1, keepdims=True)
-    s = F.round_fp16(_fp32_div(amax, 448.0))
+    s = np.minimum(F.round_fp16(_fp32_div(amax, 448.0)), F.FP16_MAX)
     with np.errstate(divide="ignore", invalid="ignore"):
         v = x / s
     c = F.e4m3_encode(np.where(s == 0, 0.0, v))

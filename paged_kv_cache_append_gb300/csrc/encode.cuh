@@ -5,11 +5,13 @@
 // "Paged KV cache" maintainer design page: the page names the profiles and
 // their plane sizes but leaves the codec rules open; the rules implemented
 // here are this library's (nk.h, nk_profile):
-//   INT8-G64  s = fp16(fp32(amax/127)), q = clamp(RNE(x/s), -127, 127)
-//   FP8-row   s = fp16(fp32(amax/448)), c = E4M3FN RNE satfinite (x/s)
+//   INT8-G64  s = min(fp16(fp32(amax/127)), 65504), q = clamp(RNE(x/s), -127, 127)
+//   FP8-row   s = min(fp16(fp32(amax/448)), 65504), c = E4M3FN RNE satfinite (x/s)
 //   NVFP4-G16 s8 = E4M3FN RNE satfinite (fp32(amax/6)), c = E2M1 RNE satfinite (x/s8)
 // fp32 quotients (__fdiv_rn) followed by one RNE conversion give the exactly
-// rounded quotient for these operand widths, so codes are bit-exact.
+// rounded quotient for these operand widths, so codes are bit-exact.  The
+// binary16 scales saturate: RNE rounding is monotone, so clamping the fp32
+// quotient at 65504 before the conversion equals clamping the rounded value.
 //
 // One warp encodes one row: lane i owns elements [i*EL, (i+1)*EL) with
 // EL = D/32, so a quantization group of 64 (or 16) elements is a run of
@@ -62,7 +64,7 @@ __device__ __forceinline__ void encode_row(const __nv_bfloat16* src, uint8_t* co
 #pragma unroll
     for (int i = 0; i < EL; ++i) a = fmaxf(a, fabsf(x[i]));
     a = group_max<LPG>(a);
-    const __half s = __float2half_rn(__fdiv_rn(a, 127.f));
+    const __half s = __float2half_rn(fminf(__fdiv_rn(a, 127.f), 65504.f));
     const float sf = __half2float(s);
     uint8_t q[EL];
 #pragma unroll
@@ -80,7 +82,7 @@ __device__ __forceinline__ void encode_row(const __nv_bfloat16* src, uint8_t* co
 #pragma unroll
     for (int i = 0; i < EL; ++i) a = fmaxf(a, fabsf(x[i]));
     a = group_max<32>(a);
-    const __half s = __float2half_rn(__fdiv_rn(a, 448.f));
+    const __half s = __float2half_rn(fminf(__fdiv_rn(a, 448.f), 65504.f));
     const float sf = __half2float(s);
     uint8_t c[EL];
 #pragma unroll

@@ -16,8 +16,10 @@ from paged_kv_cache_append_gb300 import nk
 
 pytestmark = pytest.mark.gpu
 
+# the last three put amax / 127 and amax / 448 past the largest finite
+# binary16, where the INT8-G64 and FP8-row scales saturate at 65504
 ANCHORS = [1.0, 1.0078125, 3.140625, 448.0, 449.0, 127.0, 6.0, 2688.0, 1.0e-3, 6.0e-5,
-           2.0 ** -20, 2.5e4, 1.0e6, 0.75]
+           2.0 ** -20, 2.5e4, 1.0e6, 0.75, 254 * 32768.0, 2.0 ** 26, 3.0e38]
 GROUP = {"int8_g64": 64, "fp8_row": 256, "nvfp4_g16": 16}
 
 

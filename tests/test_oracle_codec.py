@@ -181,6 +181,33 @@ def test_zero_and_tiny_groups():
     assert c[0, 0] == 0x7E and np.all(c[0, 1:] == 0x80)
 
 
+def test_binary16_scales_saturate():
+    """Closed forms above the binary16 range: amax / 127 (or / 448) past the
+    largest finite binary16 leaves s = 65504, the amax element takes the
+    extreme code, an exact multiple of s keeps its exact code, and every
+    dequantized value is finite.  Just below the edge the scale is the plain
+    rounded quotient."""
+    for amax in (253 * 32768.0, 254 * 32768.0, 2.0 ** 26, 3.0e38):
+        x = np.zeros((1, 64))
+        x[0, 5], x[0, 9] = -amax, 3 * 65504.0
+        q, sb = codec.int8_g64_quant(x)
+        s = F.fp16_from_bits(sb)[0, 0]
+        if amax / 127 < 65504:
+            assert s == 65280.0                       # 253 * 32768 / 127 = 65278 -> 65280
+            assert q[0, 5] == -127
+        else:
+            assert s == 65504.0
+            assert q[0, 5] == -127 and q[0, 9] == 3
+        assert np.all(np.isfinite(codec.int8_g64_dequant(q, sb)))
+    for amax in (2.0 ** 26, 3.0e38):
+        x = np.zeros((1, 128))
+        x[0, 0], x[0, 1] = amax, -2 * 65504.0
+        c, sb = codec.fp8_row_quant(x)
+        assert F.fp16_from_bits(sb)[0, 0] == 65504.0
+        assert c[0, 0] == 0x7E and c[0, 1] == 0xC0    # +448 (saturated), -2.0
+        assert np.all(np.isfinite(codec.fp8_row_dequant(c, sb)))
+
+
 def test_nibble_order_low_first():
     x = np.zeros((1, 16))
     x[0, 0], x[0, 1] = 6.0, -3.0             # scale 1.0 -> codes 7 and 0xD
