@@ -66,15 +66,20 @@ enum {
  * K = FP8-E4M3FN-row256 and V = NVFP4-G16).  Codec rules (the page leaves them
  * open; this library states them):
  *   BF16      codes = bf16 bits unchanged.
- *   INT8-G64  per 64 elements: s = fp16(fp32(amax/127)),
+ *   INT8-G64  per 64 elements: s = min(fp16(fp32(amax/127)), 65504),
  *             q = clamp(RNE(x/s), -127, 127); s == 0 -> q = 0.
- *   FP8-row   per (token, head) row: s = fp16(fp32(amax/448)),
+ *   FP8-row   per (token, head) row: s = min(fp16(fp32(amax/448)), 65504),
  *             c = E4M3FN RNE satfinite (x/s); s == 0 -> c = 0.
  *   NVFP4-G16 per 16 elements: s8 = E4M3FN RNE satfinite (fp32(amax/6)),
  *             c = E2M1 RNE satfinite (x/s8); s8 == 0 -> c = 0; element 2i in
  *             the low nibble of byte i.
  * Quotients are exact quotients rounded once; the sign bit of an E4M3/E2M1
- * code is the sign of its quotient. */
+ * code is the sign of its quotient.  A binary16 scale saturates at the
+ * largest finite binary16 (65504) instead of becoming +inf, as the E4M3 /
+ * E2M1 codes saturate: a group whose amax exceeds 127 * 65504 (INT8-G64) or
+ * 448 * 65504 (FP8-row) keeps s = 65504 and its large elements clamp to the
+ * extreme code, so every stored scale and every dequantized value is
+ * finite. */
 typedef enum {
   NK_BF16 = 0,
   NK_INT8_G64 = 1,
@@ -292,9 +297,12 @@ int nk_pages_from_host(nk_pool* pool, const int32_t* page_ids, int32_t n, const 
  * (row, KV head) is rejected with NK_ERR_WORKSPACE before any launch.
  * The first call on a device (with that device current, which must be the
  * pool's device) looks up the array's device address; make it before any
- * stream capture.  All calls share the array, which keeps the last call's
- * contents (every slot a call reads it writes first).  Two calls that overlap
- * on the GPU race.  Calls no allocating routine. */
+ * stream capture.  That address is kept for the life of the process, so do
+ * not use this entry point on a device after cudaDeviceReset (or any other
+ * reset of its primary context): the module is loaded again there and the
+ * kept address is stale.  All calls share the array, which keeps the last
+ * call's contents (every slot a call reads it writes first).  Two calls that
+ * overlap on the GPU race.  Calls no allocating routine. */
 int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* pool,
                                       int32_t layer, const int32_t* block_tables,
                                       const int32_t* table_rows, const int32_t* frontiers,
@@ -343,6 +351,21 @@ int nk_page_copy_columns(const nk_pool* pool, int32_t src, int32_t dst, int32_t 
  * NK_POOL_CHECK_BOUNDS, and by bounded waits that ran out).  Synchronizes
  * `stream`. */
 int nk_status_read(int32_t* status, int32_t clear, void* stream);
+
+/* Self-test of the bounded waits (no counterpart on the design pages: the
+ * pages leave failure handling of the consumer kernels open).  Every
+ * pipeline wait of this library gives up after a wall-clock limit, records
+ * NK_STATUS_TIMEOUT in the device status word and lets its kernel return, so
+ * that a lost copy never hangs the GPU.  This call launches one kernel on
+ * `stream` whose wait can never be satisfied (an mbarrier phase that expects
+ * one more arrival than it gets; no copy is involved) and that gives up after
+ * `limit_us` microseconds (1 .. 1000000).  Afterwards NK_STATUS_TIMEOUT is
+ * set in the status word of the current device (nk_status_read), and, when
+ * `waited_ns` is a device pointer, it receives the nanoseconds the wait took
+ * (-1 if the wait had completed, which cannot happen).  Asynchronous; errors:
+ * NK_ERR_INVALID_ARG for a limit outside the range, NK_ERR_CUDA on a launch
+ * failure. */
+int nk_selftest_bounded_wait(int32_t limit_us, long long* waited_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -52,7 +52,9 @@ static int make_plan(const nk_pool* p, int B, int T, int Hq, DecodePlan* pl) {
   }
   pl->target = p->num_sms * per_sm / H;
   if (pl->target < 1) pl->target = 1;
-  pl->ctas = pl->target;
+  // A budget below B (many KV heads) leaves every row one split, which still
+  // needs one CTA per row: the grid never has fewer CTAs than rows.
+  pl->ctas = pl->target > B ? pl->target : B;
   if (vfn && D <= 128) {
     // the transposed tcgen05 kernel takes several (row, page range) pieces
     // per CTA, so that equal rows still fill every SM; a row has at most
@@ -196,11 +198,15 @@ int decode_with_scratch(const void* q, int32_t Hq, const nk_pool* pool, int32_t 
       return fail(NK_ERR_WORKSPACE, "one split of this call needs " + std::to_string(per_split + fixed) +
                                         " bytes of scratch; the static scratch holds " +
                                         std::to_string(max_ws));
+    // Fewer partial slots per (row, KV head).  The slot count bounds the
+    // splits of the plan (a budget below B gives every row one split, which
+    // writes its output directly); the CTA count must still cover the splits,
+    // so it never drops below B.
     pl.target = static_cast<int>(fit < static_cast<size_t>(pl.target) ? fit : pl.target);
     if (pl.nseg > 0) {
       if (pl.nseg > pl.target) pl.nseg = pl.target;  // every row's pieces still fit its slots
     } else {
-      pl.ctas = pl.target;
+      pl.ctas = pl.target > B ? pl.target : B;
     }
     plan_sizes(&pl, B, H, D);
   }

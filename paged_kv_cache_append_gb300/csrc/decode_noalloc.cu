@@ -14,9 +14,13 @@
 // where the GPU can reach host memory.  So the first call on a device, with
 // that device current, asks the runtime for the array's device address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture.  All calls share the array and it keeps the last call's contents;
-// every slot of split partials a call reads it wrote first, so nothing needs
-// clearing.  Two calls that overlap on the GPU race on the array.
+// capture.  The cached address lives as long as the process: after a reset
+// of the device's primary context (cudaDeviceReset) the module is loaded
+// again and the cached address is stale, so the entry point must not be used
+// across such a reset.  All calls share the array and it keeps the last
+// call's contents; every slot of split partials a call reads it wrote first,
+// so nothing needs clearing.  Two calls that overlap on the GPU race on the
+// array.
 #include <mutex>
 
 #include "internal.h"

@@ -11,6 +11,7 @@ import numpy as np
 import torch
 
 from oracle import attention as OA
+from oracle import codec as OC
 from oracle import formats as OF
 from oracle.store import PoolImage
 from paged_kv_cache_append_gb300 import nk
@@ -141,19 +142,40 @@ class Scenario:
         return bad
 
 
+def oracle_row(w: Workload, layer: int, b: int):
+    """Oracle (out [T, Hq, D], lse [T, Hq]) of decode row b after its step
+    append, from the host inputs alone: encodes only that row's context and
+    step tokens (rows that share a prefix read row 0's values there)."""
+    r = int(w.table_rows[b])
+    n = int(w.context[b])
+    sh = w.shared_len
+    kc, vc = w.context_kv(layer, r, n)
+    if sh and r != 0:
+        k0, v0 = w.context_kv(layer, 0, int(w.context[0]))
+        kc = torch.cat([k0[:sh], kc[sh:]])
+        vc = torch.cat([v0[:sh], vc[sh:]])
+    ks, vs = w.step_kv(layer)
+    kb = np.concatenate([bf16_to_bits(kc), bf16_to_bits(ks[b])], axis=0)
+    vb = np.concatenate([bf16_to_bits(vc), bf16_to_bits(vs[b])], axis=0)
+    K, V = OC.decode_kv(w.profile, OC.encode_kv(w.profile, kb, vb))
+    q = OF.bf16_bits_to_f64(bf16_to_bits(w.step_q(layer)[b]))
+    return OA.decode(q, K, V, n + w.T, w.scale)
+
+
 def compare_attention(out, lse, ref_out, ref_lse, atol_out=2e-2, atol_lse=1e-3, strict=False):
     """Checks the GPU output against the oracle.
 
-    out: |gpu - oracle| <= 2e-2 + 2^-7 |oracle|, i.e. 2e-2 absolute beyond one
-    bf16 ulp of the output (a bf16 value of magnitude |o| is itself rounded
-    by up to 2^-8 |o|, which alone exceeds 2e-2 once |o| > 5).
+    out: |gpu - oracle| <= 2e-2 + 2^-8 |oracle|, i.e. 2e-2 absolute beyond the
+    rounding of the bf16 output itself (round to nearest moves a value of
+    magnitude |o| by at most half an ulp, 2^-8 |o|, which alone exceeds 2e-2
+    once |o| > 5, as with the x20 outliers).
     lse: |gpu - oracle| <= 1e-3 where finite; -inf exactly where the oracle
     has no key.  strict=True drops the ulp term (plain 2e-2 absolute).
     Returns (max out excess, max lse error)."""
     o = out.float().numpy().astype(np.float64)
     l = lse.numpy().astype(np.float64)
     assert np.all(np.isfinite(o)), "non-finite output"
-    excess = np.abs(o - ref_out) - (0.0 if strict else 2.0 ** -7) * np.abs(ref_out)
+    excess = np.abs(o - ref_out) - (0.0 if strict else 2.0 ** -8) * np.abs(ref_out)
     err_o = float(np.max(excess)) if o.size else 0.0
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(l), fin), "lse finiteness differs"

@@ -366,3 +366,19 @@ def test_wide_query_groups_at_head_dim_256_need_exact_f16_codes():
             sc.gpu.decode(0, w.step_q(0).to(dev), sc.tables_d, torch.from_numpy(w.table_rows).to(dev),
                           torch.from_numpy(w.context + 4).to(dev), w.scale)
         assert e.value.code == -4   # NK_ERR_UNSUPPORTED
+
+
+# ---- many KV heads: a per-head split budget below the number of rows ------------
+@pytest.mark.parametrize("profile,Hkv,G,D,T", [
+    ("fp8_row", 24, 8, 256, 4),     # tcgen05 quadrant kernel, one CTA per SM: 152 / 24 = 6 < 8 rows
+    ("k8v4", 40, 8, 128, 4),        # transposed tcgen05 kernel (pieces): 152 / 40 = 3 < 8 rows
+    ("int8_g64", 64, 8, 256, 1),    # warp-level kernel at D 256: (152 x CTAs per SM) / 64 < 8 rows
+], ids=["quadrant", "pieces", "warp_level"])
+@pytest.mark.parametrize("fused", [False, True], ids=["append_then_decode", "fused"])
+def test_many_kv_heads_still_cover_every_row(profile, Hkv, G, D, T, fused):
+    """With so many KV heads that the SMs give each head fewer CTAs than the
+    batch has rows, every row still runs (one split each) and matches the
+    oracle; no row is left unwritten."""
+    w = small(profile, Hkv, G, D, 256, 8, T, seed=Hkv + D + T,
+              contexts=[0, 60, 100, 127, 190, 200, 250 - T, 63])
+    run_and_check(w, fused=fused)
