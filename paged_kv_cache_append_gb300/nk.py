@@ -32,7 +32,7 @@ SYMBOLS = ["nk_version", "nk_last_error", "nk_pool_plane_bytes", "nk_pool_capaci
            "nk_paged_decode_attention_noalloc",
            "nk_prefill_workspace_bytes", "nk_paged_prefill_attention",
            "nk_page_copy_columns", "nk_status_read", "nk_host_page_bytes", "nk_page_runs",
-           "nk_pages_to_host", "nk_pages_from_host"]
+           "nk_pages_to_host", "nk_pages_from_host", "nk_selftest_bounded_wait"]
 
 
 class NkError(RuntimeError):
@@ -83,6 +83,7 @@ def load(path: str | None = None) -> C.CDLL:
         "nk_paged_prefill_attention": (C.c_int, [_P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _F, _P, _P, _P, _S, _P]),
         "nk_page_copy_columns": (C.c_int, [_P, _I, _I, _I, _P]),
         "nk_status_read": (C.c_int, [C.POINTER(_I), _I, _P]),
+        "nk_selftest_bounded_wait": (C.c_int, [_I, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -212,6 +213,10 @@ def nk_status_read(clear: bool = True, stream=None) -> int:
     s = _I()
     _check(load().nk_status_read(C.byref(s), int(clear), stream))
     return s.value
+
+
+def nk_selftest_bounded_wait(limit_us: int, waited_ns_ptr=None, stream=None) -> None:
+    _check(load().nk_selftest_bounded_wait(int(limit_us), waited_ns_ptr, stream))
 
 
 # ------------------------------------------------------------ torch wrapper
