@@ -309,15 +309,17 @@ int nk_paged_decode_attention_noalloc(const void* q, int32_t Hq, const nk_pool* 
                                       int32_t B, int32_t T, float softmax_scale, void* out,
                                       float* lse, void* stream);
 
-/* Workspace the prefill call needs (may be 0). */
+/* Workspace the prefill call needs (may be 0).  It depends on B, Tc, Hq, the
+ * KV heads and D only, never on the pool's context length. */
 int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32_t Hq,
                                size_t* bytes);
 
 /* Chunked prefill / replay attention through the block tables (every
- * profile; quantized pages are first converted by their own launch into f16
- * tiles, which the tensor-core launch then reads.  The tiles hold FP8-row,
- * NVFP4-G16 and K8V4 values exactly; INT8-G64 values, code times group
- * scale, are rounded once to f16, relative error <= 2^-11).
+ * profile; quantized pages are dequantized inside the tensor-core kernel,
+ * page tile by page tile in shared memory, with no copy of the context
+ * elsewhere.  The tiles hold FP8-row, NVFP4-G16 and K8V4 values exactly;
+ * INT8-G64 values, code times group scale, are rounded once to f16, relative
+ * error <= 2^-11).
  * Query i < chunk_len[b] of row b sits at logical position prefix_len[b] + i
  * and attends keys j <= prefix_len[b] + i; the chunk's own K/V must already
  * be appended.  Prefill work is proportional to prefix*S + S(S+1)/2 query-key
@@ -326,9 +328,9 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
  *   (rows i >= chunk_len[b] are not written);  lse: device fp32 [B][Tc][Hq]
  *   or NULL;  prefix_len, chunk_len: device int32 [B], chunk_len[b] <= Tc.
  *   workspace: nk_prefill_workspace_bytes bytes, zero-filled before its first
- *   use (every call leaves its counters at zero): the dequant scratch of
- *   quantized pools and, when the launch splits each 128-row tile over its
- *   pages to fill the last wave of SMs, the split partials and counters.
+ *   use (every call leaves its counters at zero): when the launch splits each
+ *   128-row tile over its pages to fill the last wave of SMs, the split
+ *   partials and counters.
  * Errors as for decode; NK_ERR_UNSUPPORTED for D other than 64, 128 and 256,
  * or a GQA group that does not divide 128 or exceeds 16. */
 int nk_paged_prefill_attention(const void* q_chunk, int32_t Hq, const nk_pool* pool,

@@ -392,7 +392,6 @@ namespace nk {
 int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* tables, const int32_t* table_rows,
                     const int32_t* prefix_len, const int32_t* chunk_len, int B, int Tc, int Hq, float scale_log2,
                     void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t s);
-size_t qprefill_workspace_bytes(const nk_pool* p, int B);
 }  // namespace nk
 
 using namespace nk;
@@ -402,15 +401,14 @@ extern "C" int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_
   clear_error();
   if (!pool || !bytes) return fail(NK_ERR_INVALID_ARG, "null argument");
   if (Hq < 1 || Hq % pool->desc.num_kv_heads || Tc < 1 || B < 1) return fail(NK_ERR_SHAPE, "bad B, Tc or Hq");
-  // quantized pools: the f16 scratch of the dequant pass; then, when the
-  // tiles are split over their pages, the partials and counters (zero-filled
-  // before the first use, left at zero by every call)
+  // every profile: when the tiles are split over their pages, the partials
+  // and counters (zero-filled before the first use, left at zero by every
+  // call); the size depends on B, H, Tc and D, never on the context
   const int H = pool->desc.num_kv_heads, G = Hq / H;
   if (G > 16 || 128 % G) return fail(NK_ERR_UNSUPPORTED, "GQA group must divide 128 and be <= 16");
   const int tiles = (Tc + 128 / G - 1) / (128 / G);
   const int nsplit = prefill_nsplit(tiles * H * B, pool->num_sms);
-  *bytes = (qprefill_workspace_bytes(pool, B) + 255) / 256 * 256 +
-           prefill_split_bytes(B, H, tiles, nsplit, pool->desc.head_dim);
+  *bytes = prefill_split_bytes(B, H, tiles, nsplit, pool->desc.head_dim);
   return NK_OK;
 }
 

@@ -2,24 +2,34 @@
 // the 5th-generation tensor cores: INT8-G64, FP8-E4M3FN-row256, NVFP4-G16 and
 // K8V4 (FP8-row K, NVFP4 V) pools.
 //
-// Two launches, split by what bounds them:
-//   1. qdequant_kernel (HBM bound) converts each page of the prefill rows
-//      once into an f16 scratch in logical page order, with per-key fp32
-//      scales; pages past a row's frontier are not touched, rows past it are
-//      zero.  Every CTA of the tensor pass would otherwise re-convert the same
-//      pages (128 query rows share each page), which made the conversion,
-//      not the tensor cores, the bound.
-//   2. qprefill_kernel (tensor bound) is the BF16 prefill (prefill.cu) on
-//      f16 operands: K and V page tiles come from the scratch by TMA, Q and P
-//      live in TMEM, and the per-key scales multiply the fp32 scores (K) and
-//      the softmax weights (V).
+// The pages are read in place through the block table and dequantized inside
+// the attention kernel, page tile by page tile, in shared memory ("Paged KV
+// cache" maintainer design page, consumer view: no gather to a contiguous
+// cache and no staging copy whose size grows with the context).  One CTA owns
+// 128 query rows of one (row b, KV head h), as in the BF16 prefill
+// (prefill.cu):
+//   warp 4      TMA producer: the raw code tile of each page (the pool's own
+//               tensor maps, 64 rows x min(row bytes, 128) boxes) and its
+//               scale tile (bulk copy) into a raw K ring and a raw V ring;
+//   warps 6-9   converters: each page's codes become an f16 tile in the
+//               layout the MMAs read (rows = keys, 128-byte rows of 64 dims,
+//               128-byte swizzle), K one page ahead of V; with the V tile
+//               they store each key's fp32 factors (K: score factor times
+//               softmax_scale * log2 e; V: softmax weight factor);
+//   warp 5      MMA issuer: S = Q K^T (A = Q in TMEM, B = the f16 K tile),
+//               O += P V (A = P in TMEM, B = the f16 V tile, MN-major);
+//   warps 0-3   Q to TMEM (f16, each query row prescaled by a power of two),
+//               online softmax with the per-key factors, epilogue.
+// Per page the raw codes cross HBM / L2 once per CTA; the f16 tiles never
+// leave the SM.
+//
 // Every operand is exact ("Paged KV cache" page: dequantization belongs to
 // the attention consumer; the codec rules are this library's, nk.h):
 //   * E4M3 and E2M1 codes are exact binary16 values, and an E2M1 code times
 //     its E4M3 group scale is an exact binary16 product (at most 6
 //     significant bits, within range), so NVFP4 pages become exact f16 values;
 //   * FP8-row pages keep their codes, and the row scale of each key is applied
-//     in fp32;
+//     in fp32 to its score (K) and its softmax weight (V);
 //   * q is scaled per query row by a power of two, 2^e with max|q| 2^e in
 //     [2^14, 2^15), which makes bf16 -> f16 exact for every element above
 //     max|q| 2^-31; the scores divide 2^e back out in fp32.
@@ -29,17 +39,14 @@
 // an INT8 code (7 bits) times its binary16 group scale (11 bits) needs up to
 // 18 significant bits, and an exact form would need one fp32 accumulator per
 // 64-dim group of each key, four times the S columns of tensor memory.  Its
-// pages are dequantized as code * s_g computed exactly in fp32 and rounded
+// codes are dequantized as code * s_g computed exactly in fp32 and rounded
 // once to f16 (relative error <= 2^-11 per element), after a per-key power
 // of two 2^-e, e in [0, 7], that keeps the largest element of the key below
-// 2^15; 2^e goes into the key's fp32 factor (K) or its softmax weight (V),
-// which stays below 2^8 * 2^7 under the lazy 2^8 threshold.  Scores then
-// differ from the exact ones by at most 2^-11 of sum_d |q_d k_d| times the
-// softmax scale, well inside the attention tolerances.
-//
-// Scratch (the call's workspace): K f16 [B][H][L][64][D], V f16 likewise,
-// scales fp32 [B][H][L][128] (64 K scales times softmax_scale * log2 e, then
-// 64 V scales; 0 for keys past the frontier).
+// 2^15 (every binary16 scale is at most 65504, so every key fits f16); 2^e
+// goes into the key's fp32 factor (K) or its softmax weight (V), which stays
+// below 2^8 * 2^7 under the lazy 2^8 threshold.  Scores then differ from the
+// exact ones by at most 2^-11 of sum_d |q_d k_d| times the softmax scale, well
+// inside the attention tolerances.
 #include <cmath>
 
 #include "encode.cuh"
@@ -49,33 +56,14 @@
 
 namespace nk {
 
-struct QScratch {
-  __half* k;
-  __half* v;
-  float* sc;
-  static size_t bytes(int B, int H, int L, int D) {
-    const size_t pages = static_cast<size_t>(B) * H * L;
-    return pages * 64 * D * 2 * 2 + pages * 128 * 4;
-  }
-  static QScratch at(void* ws, int B, int H, int L, int D) {
-    const size_t pages = static_cast<size_t>(B) * H * L;
-    char* p = static_cast<char*>(ws);
-    return QScratch{reinterpret_cast<__half*>(p), reinterpret_cast<__half*>(p + pages * 64 * D * 2),
-                    reinterpret_cast<float*>(p + pages * 64 * D * 4)};
-  }
-};
-
 struct QArgs {
   const __nv_bfloat16* q;  // [B][Tc][Hq][D]
   const int32_t* tables;
   const int32_t* table_rows;
   const int32_t* prefix_len;
   const int32_t* chunk_len;
-  const uint8_t* kc;  // layer planes: K codes, V codes, K scales, V scales
-  const uint8_t* vc;
-  const uint8_t* ks;
+  const uint8_t* ks;  // layer scale planes: K scales, V scales
   const uint8_t* vs;
-  QScratch scr;
   __nv_bfloat16* out;
   float* lse;
   int* status;
@@ -86,16 +74,8 @@ struct QArgs {
   int head_major;  // plane order
 };
 
-// Row geometry shared by both passes; false when the row is malformed.
-__device__ __forceinline__ bool q_row(const QArgs& a, int b, int& row, int& prefix, int& chunk) {
-  row = a.table_rows[b];
-  prefix = a.prefix_len[b];
-  chunk = a.chunk_len[b];
-  return !(row < 0 || row >= a.C || prefix < 0 || chunk < 0 || chunk > a.Tc ||
-           static_cast<int64_t>(prefix) + chunk > static_cast<int64_t>(a.L) * 64);
-}
-
-// INT8-G64 rows: the power of two e (0..7) with 127 * max_g s_g * 2^-e < 2^15.
+// INT8-G64 keys: the power of two e (0..7) with 127 * max_g s_g * 2^-e < 2^15
+// (or the largest, 7, when binary16's range forbids it).
 template <int D>
 __device__ __forceinline__ int int8_row_shift(const uint8_t* scale_row) {
   float smax = 0.f;
@@ -107,96 +87,37 @@ __device__ __forceinline__ int int8_row_shift(const uint8_t* scale_row) {
   return min(max(ex - 15, 0), 7);
 }
 
-// 8 dims [d, d + 8) of one token-head row -> 8 f16 values (16 bytes): exact
-// for FP8 and NVFP4; for INT8-G64, code * s_g * 2^-e rounded once.
-template <int KIND, int D>
-__device__ __forceinline__ uint4 dequant8(const uint8_t* code_row, const uint8_t* scale_row, int d) {
-  if constexpr (KIND == KIND_INT8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(code_row + d);
-    const float sg = ldexpf(__half2float(*reinterpret_cast<const __half*>(scale_row + 2 * (d / 64))),
-                            -int8_row_shift<D>(scale_row));
-    const int8_t* c = reinterpret_cast<const int8_t*>(&w);
-    uint32_t h[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = pack_f16x2(static_cast<float>(c[2 * i]) * sg, static_cast<float>(c[2 * i + 1]) * sg);
-    return make_uint4(h[0], h[1], h[2], h[3]);
-  } else if constexpr (KIND == KIND_FP8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(code_row + d);
-    return make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
-                      e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
-                      e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xFFFFu)),
-                      e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
-  } else {  // NVFP4: 4 bytes of codes times the group's E4M3 scale
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(code_row + d / 2);
-    const uint32_t s16 = e4m3x2_to_f16x2(static_cast<uint16_t>(scale_row[d / 16])) & 0xFFFFu;
-    const uint32_t s2 = s16 | (s16 << 16);
-    return make_uint4(hmul2_u32(e2m1x2_byte_to_f16x2<0>(w), s2), hmul2_u32(e2m1x2_byte_to_f16x2<1>(w), s2),
-                      hmul2_u32(e2m1x2_byte_to_f16x2<2>(w), s2), hmul2_u32(e2m1x2_byte_to_f16x2<3>(w), s2));
-  }
-}
-
-// ------------------------------------------------------------------ pass 1
 template <int KK, int KV, int D>
-__global__ void __launch_bounds__(128) qdequant_kernel(QArgs a) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  int row, prefix, chunk;
-  if (!q_row(a, b, row, prefix, chunk)) return;  // the tensor pass reports it
-  const int F = prefix + chunk;
-  if (p >= (F + 63) / 64) return;
-  int g = a.tables[static_cast<int64_t>(row) * a.L + p];
-  if (g < 0 || g >= a.M) {  // never read outside the pool
-    if (tid == 0) set_status(a.status, NK_STATUS_PAGE_RANGE);
-    g = -1;
-  }
-  constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
-  constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
-  const int kvalid = g < 0 ? 0 : F - 64 * p;            // rows >= kvalid are stale: zeros
-  const int64_t src = g < 0 ? 0 : tile_row(g, h, a.H, a.M, a.head_major);
-  const int64_t dst = ((static_cast<int64_t>(b) * a.H + h) * a.L + p) * 64;
-  for (int c = tid; c < 64 * (D / 8); c += 128) {
-    const int r = c / (D / 8), d = (c % (D / 8)) * 8;
-    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-    if (r < kvalid) {
-      kv = dequant8<KK, D>(a.kc + (src + r) * KCB, a.ks + (src + r) * KSB, d);
-      vv = dequant8<KV, D>(a.vc + (src + r) * VCB, a.vs + (src + r) * VSB, d);
-    }
-    *reinterpret_cast<uint4*>(a.scr.k + (dst + r) * D + d) = kv;
-    *reinterpret_cast<uint4*>(a.scr.v + (dst + r) * D + d) = vv;
-  }
-  if (tid < 64) {
-    float ksc = 0.f, vsc = 0.f;
-    if (tid < kvalid) {
-      if constexpr (KK == KIND_FP8) ksc = __half2float(*reinterpret_cast<const __half*>(a.ks + (src + tid) * KSB));
-      else if constexpr (KK == KIND_INT8) ksc = ldexpf(1.f, int8_row_shift<D>(a.ks + (src + tid) * KSB));
-      else ksc = 1.f;
-      if constexpr (KV == KIND_FP8) vsc = __half2float(*reinterpret_cast<const __half*>(a.vs + (src + tid) * VSB));
-      else if constexpr (KV == KIND_INT8) vsc = ldexpf(1.f, int8_row_shift<D>(a.vs + (src + tid) * VSB));
-      else vsc = 1.f;
-    }
-    float* sc = a.scr.sc + (dst / 64) * 128;
-    sc[tid] = ksc * a.scale_log2;
-    sc[64 + tid] = vsc;
-  }
-}
-
-// ------------------------------------------------------------------ pass 2
-template <int D>
 struct QCfg {
-  static constexpr int THREADS = 192;
-  static constexpr int NK = D == 256 ? 3 : 6;
-  static constexpr int NV = D == 256 ? 3 : 6;
-  static constexpr int KV_BYTES = 64 * D * 2;                 // one f16 page tile
-  static constexpr int V_STAGE = KV_BYTES + 1024;             // + the page's 128 scales (512 B)
-  static constexpr int OFF_V = NK * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
-  static constexpr int NBAR = 2 * NK + 2 * NV + 2 + 4;
+  static constexpr int THREADS = 320;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-9 converters
+  static constexpr int NCONV = 4;      // converter warps
+  static constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
+  static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
+  static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
+  static constexpr int F16 = 64 * D * 2;                           // one f16 page tile
+  static constexpr int K_STAGE = F16;
+  static constexpr int V_STAGE = F16 + 1024;                       // + 128 fp32 factors per key
+  static constexpr int RK_CODES = (64 * KCB + 1023) / 1024 * 1024;  // raw K code tile (1024-aligned)
+  static constexpr int RV_CODES = (64 * VCB + 1023) / 1024 * 1024;
+  static constexpr int RK_STAGE = (RK_CODES + 64 * KSB + 1023) / 1024 * 1024;
+  static constexpr int RV_STAGE = (RV_CODES + 64 * VSB + 1023) / 1024 * 1024;
+  static constexpr int NK = D == 256 ? 2 : D == 128 ? 4 : 6;  // f16 K ring
+  static constexpr int NV = NK;                                // f16 V ring
+  static constexpr int NRK = D == 256 ? (RK_STAGE <= 10240 ? 3 : 2) : 4;  // raw rings
+  static constexpr int NRV = D == 256 ? (RV_STAGE <= 10240 ? 3 : 2) : 4;
+  static constexpr int OFF_V = NK * K_STAGE;
+  static constexpr int OFF_RK = OFF_V + NV * V_STAGE;
+  static constexpr int OFF_RV = OFF_RK + NRK * RK_STAGE;
+  static constexpr int OFF_BAR = OFF_RV + NRV * RV_STAGE;
+  static constexpr int NBAR = 2 * NK + 2 * NV + 2 * NRK + 2 * NRV + 2 + 4;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 64 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0, COL_Q = 128, COL_O = 256;
   static constexpr uint32_t ID_S = tc::idesc_f16(128, 64, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
+  static constexpr int UNITS = 64 * (D / 16);  // (key, 16-dim group) units of a tile
+  static constexpr int UPT = UNITS / (32 * NCONV);  // units per converter thread
+  static_assert(UPT * 32 * NCONV == UNITS, "converter units");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -204,21 +125,118 @@ __device__ __forceinline__ void q_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <int D>
-__global__ void __launch_bounds__(192, 1)
+// Byte address (offset in the raw tile) of byte `col` of key row r in a tile
+// staged as blocks of 64 rows x RB bytes with the matching TMA swizzle.
+template <int RB>
+__device__ __forceinline__ uint32_t raw_off(int r, int col) {
+  return static_cast<uint32_t>((col / RB) * (64 * RB)) + swz<RB>(r, col % RB);
+}
+
+// Offset of f16 element (key r, dim d) in an f16 tile: 64-dim blocks of
+// 64 rows x 128 bytes, 128-byte swizzle (d a multiple of 8: a 16-byte chunk).
+__device__ __forceinline__ uint32_t f16_off(int r, int d) {
+  return static_cast<uint32_t>((d >> 6) * 8192) + swz<128>(r, (d & 63) * 2);
+}
+
+// 16 dims [16 g, 16 g + 16) of key r: raw codes and scales (shared memory) ->
+// 16 f16 values (two 16-byte chunks).  `shift` is the INT8 key's 2^-e.
+template <int KIND, int D, int RB>
+__device__ __forceinline__ void convert16(const uint8_t* codes, const uint8_t* scales, int r, int g, float shift,
+                                          uint4& lo, uint4& hi) {
+  constexpr int SB = scale_row_bytes<KIND>(D);
+  if constexpr (KIND == KIND_FP8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(codes + raw_off<RB>(r, 16 * g));
+    lo = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xFFFFu)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xFFFFu)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+    hi = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z & 0xFFFFu)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.w & 0xFFFFu)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
+  } else if constexpr (KIND == KIND_INT8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(codes + raw_off<RB>(r, 16 * g));
+    const float sg = __half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * g) / 64))) * shift;
+    const int8_t* c = reinterpret_cast<const int8_t*>(&w);
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      h[i] = pack_f16x2(static_cast<float>(c[2 * i]) * sg, static_cast<float>(c[2 * i + 1]) * sg);
+    lo = make_uint4(h[0], h[1], h[2], h[3]);
+    hi = make_uint4(h[4], h[5], h[6], h[7]);
+  } else {  // NVFP4: 8 bytes of codes times the group's E4M3 scale
+    const uint2 w = *reinterpret_cast<const uint2*>(codes + raw_off<RB>(r, 8 * g));
+    const uint32_t s16 = e4m3x2_to_f16x2(static_cast<uint16_t>(scales[r * SB + g])) & 0xFFFFu;
+    const uint32_t s2 = s16 | (s16 << 16);
+    lo = make_uint4(hmul2_u32(e2m1x2_byte_to_f16x2<0>(w.x), s2), hmul2_u32(e2m1x2_byte_to_f16x2<1>(w.x), s2),
+                    hmul2_u32(e2m1x2_byte_to_f16x2<2>(w.x), s2), hmul2_u32(e2m1x2_byte_to_f16x2<3>(w.x), s2));
+    hi = make_uint4(hmul2_u32(e2m1x2_byte_to_f16x2<0>(w.y), s2), hmul2_u32(e2m1x2_byte_to_f16x2<1>(w.y), s2),
+                    hmul2_u32(e2m1x2_byte_to_f16x2<2>(w.y), s2), hmul2_u32(e2m1x2_byte_to_f16x2<3>(w.y), s2));
+  }
+}
+
+// Factor of key r of a raw tile: FP8-row its row scale, INT8-G64 its 2^e,
+// NVFP4 1 (the scales are inside the f16 values).
+template <int KIND, int D>
+__device__ __forceinline__ float key_factor(const uint8_t* scales, int r) {
+  constexpr int SB = scale_row_bytes<KIND>(D);
+  if constexpr (KIND == KIND_FP8) return __half2float(*reinterpret_cast<const __half*>(scales + r * SB));
+  else if constexpr (KIND == KIND_INT8) return ldexpf(1.f, int8_row_shift<D>(scales + r * SB));
+  else return 1.f;
+}
+
+// One converter thread's share of a page tile: units (key r, 16-dim group g)
+// u = ct + 128 k; keys at or past `kvalid` become zeros.
+template <int KIND, int D, int RB>
+__device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, uint8_t* f16, int ct, int kvalid) {
+  constexpr int GPR = D / 16;  // 16-dim groups per key
+  constexpr int UPT = (64 * GPR) / 128;
+  constexpr int SB = scale_row_bytes<KIND>(D);
+  const uint8_t* scales = raw + raw_codes;
+  uint4 lo[UPT], hi[UPT];
+  int rr[UPT], gg[UPT];
+#pragma unroll
+  for (int k = 0; k < UPT; ++k) {
+    const int u = ct + 128 * k;
+    rr[k] = (u & 7) + 8 * ((u >> 3) / GPR);
+    gg[k] = (u >> 3) % GPR;
+  }
+  // every raw load of the thread before any store (the stores could alias)
+#pragma unroll
+  for (int k = 0; k < UPT; ++k) {
+    float shift = 1.f;
+    if constexpr (KIND == KIND_INT8) shift = ldexpf(1.f, -int8_row_shift<D>(scales + rr[k] * SB));
+    convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < UPT; ++k) {
+    if (rr[k] >= kvalid) lo[k] = hi[k] = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k])) = lo[k];
+    *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k] + 8)) = hi[k];
+  }
+}
+
+template <int KK, int KV, int D>
+__global__ void __launch_bounds__(320, 1)
     qprefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, QArgs a) {
-  using Cfg = QCfg<D>;
-  constexpr int NK = Cfg::NK, NV = Cfg::NV;
+  using Cfg = QCfg<KK, KV, D>;
+  constexpr int NK = Cfg::NK, NV = Cfg::NV, NRK = Cfg::NRK, NRV = Cfg::NRV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::OFF_V;
+  uint8_t* sRK = smem + Cfg::OFF_RK;
+  uint8_t* sRV = smem + Cfg::OFF_RV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  uint64_t* k_full = bars;
-  uint64_t* k_empty = k_full + NK;
-  uint64_t* v_full = k_empty + NK;
-  uint64_t* v_empty = v_full + NV;
-  uint64_t* s_full = v_empty + NV;  // [2]
+  uint64_t* k_full = bars;             // f16 K tile ready (converters)
+  uint64_t* k_empty = k_full + NK;     // S of the tile done (MMA commit)
+  uint64_t* v_full = k_empty + NK;     // f16 V tile + factors ready (converters)
+  uint64_t* v_empty = v_full + NV;     // PV of the tile done (MMA commit)
+  uint64_t* rk_full = v_empty + NV;    // raw K tile landed (TMA)
+  uint64_t* rk_empty = rk_full + NRK;  // raw K tile converted
+  uint64_t* rv_full = rk_empty + NRK;
+  uint64_t* rv_empty = rv_full + NRV;
+  uint64_t* s_full = rv_empty + NRV;  // [2]
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 1;
   uint64_t* q_ready = o_done + 1;
@@ -231,11 +249,13 @@ __global__ void __launch_bounds__(192, 1)
   const int qt = blockIdx.x / a.sp.nsplit, split = blockIdx.x % a.sp.nsplit;
   const int h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, TQ = 128 / G;
-  griddep_wait();  // the dequant pass has completed
+  griddep_wait();  // launched with programmatic stream serialization
   griddep_launch_dependents();
 
-  int row, prefix, chunk;
-  if (!q_row(a, b, row, prefix, chunk)) {
+  const int row = a.table_rows[b];
+  const int prefix = a.prefix_len[b], chunk = a.chunk_len[b];
+  if (row < 0 || row >= a.C || prefix < 0 || chunk < 0 || chunk > a.Tc ||
+      static_cast<int64_t>(prefix) + chunk > static_cast<int64_t>(a.L) * 64) {
     if (tid == 0 && qt == 0 && h == 0) set_status(a.status, NK_STATUS_FRONTIER);
     return;
   }
@@ -247,16 +267,25 @@ __global__ void __launch_bounds__(192, 1)
   const int per = (nkt + a.sp.nsplit - 1) / a.sp.nsplit;
   const int p_lo = min(split * per, nkt);
   const int n = min(p_lo + per, nkt) - p_lo;
-  const int page0 = (b * a.H + h) * a.L + p_lo;  // scratch page of local page 0
+  const int F = prefix + chunk;  // keys >= F of a page are stale
+  const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L + p_lo;
 
   if (tid == 0) {
     for (int i = 0; i < NK; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], Cfg::NCONV);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < NV; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], Cfg::NCONV);
       mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < NRK; ++i) {
+      mbar_init(&rk_full[i], 1);
+      mbar_init(&rk_empty[i], Cfg::NCONV);
+    }
+    for (int i = 0; i < NRV; ++i) {
+      mbar_init(&rv_full[i], 1);
+      mbar_init(&rv_empty[i], Cfg::NCONV);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
@@ -279,36 +308,104 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tslot;
 
   if (warp == 4) {
-    // -------- TMA producer: f16 K / V tiles and the scales of each page --------
-    if (lane == 0) {
-      for (int j = 0; j < n; ++j) {
-        const int y = (page0 + j) * 64;
-        const int ks = j % NK, vs = j % NV;
-        if (j >= NK && !mbar_wait_bounded(&k_empty[ks], ((j / NK) - 1) & 1, a.status)) break;
-        mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
+    // ------------- TMA producer: raw code and scale tiles of each page -----------
+    int gnext = 0;
+    for (int j = 0; j < n; ++j) {
+      if ((j & 31) == 0) gnext = (j + lane < n) ? table[j + lane] : 0;
+      int g = __shfl_sync(0xffffffffu, gnext, j & 31);
+      int stop = 0;
+      if (lane == 0) {
+        if (g < 0 || g >= a.M) {  // never copy from outside the pool
+          set_status(a.status, NK_STATUS_PAGE_RANGE);
+          g = 0;
+        }
+        const int y = static_cast<int>(tile_row(g, h, a.H, a.M, a.head_major));
+        const int rk = j % NRK, rv = j % NRV;
+        if (j >= NRK && !mbar_wait_bounded(&rk_empty[rk], ((j / NRK) - 1) & 1, a.status)) stop = 1;
+        if (!stop) {
+          uint8_t* st = sRK + rk * Cfg::RK_STAGE;
+          mbar_arrive_expect_tx(&rk_full[rk], 64 * Cfg::KCB + 64 * Cfg::KSB);
 #pragma unroll
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sK + ks * Cfg::KV_BYTES + kb * 8192, &tmk, kb * 128, y, &k_full[ks]);
-        if (j >= NV && !mbar_wait_bounded(&v_empty[vs], ((j / NV) - 1) & 1, a.status)) break;
-        uint8_t* vst = sV + vs * Cfg::V_STAGE;
-        mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES + 512);
+          for (int c = 0; c < Cfg::KCB / Cfg::K_RB; ++c)
+            tma_load_2d(st + c * 64 * Cfg::K_RB, &tmk, c * Cfg::K_RB, y, &rk_full[rk]);
+          bulk_load(st + Cfg::RK_CODES, a.ks + static_cast<int64_t>(y) * Cfg::KSB, 64 * Cfg::KSB, &rk_full[rk]);
+        }
+        if (!stop && j >= NRV && !mbar_wait_bounded(&rv_empty[rv], ((j / NRV) - 1) & 1, a.status)) stop = 1;
+        if (!stop) {
+          uint8_t* st = sRV + rv * Cfg::RV_STAGE;
+          mbar_arrive_expect_tx(&rv_full[rv], 64 * Cfg::VCB + 64 * Cfg::VSB);
 #pragma unroll
-        for (int kb = 0; kb < D / 64; ++kb) tma_load_2d(vst + kb * 8192, &tmv, kb * 128, y, &v_full[vs]);
-        bulk_load(vst + Cfg::KV_BYTES, a.scr.sc + static_cast<int64_t>(page0 + j) * 128, 512, &v_full[vs]);
+          for (int c = 0; c < Cfg::VCB / Cfg::V_RB; ++c)
+            tma_load_2d(st + c * 64 * Cfg::V_RB, &tmv, c * Cfg::V_RB, y, &rv_full[rv]);
+          bulk_load(st + Cfg::RV_CODES, a.vs + static_cast<int64_t>(y) * Cfg::VSB, 64 * Cfg::VSB, &rv_full[rv]);
+        }
+        if (stop) *s_abort = 1;
       }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
     }
+  } else if (warp >= 6) {
+    // ------------- converters: K one page ahead of V ------------------------------
+    // Order K(0), K(1), V(0), K(2), V(1), ...: the MMA issues S(i) before
+    // PV(i - 1).  Thread ct < 64 carries key ct's K factor from K(i) to the
+    // factor slot of V(i), which is written with the V tile.
+    const int ct = tid - 192;  // 0..127
+    float kf_prev = 0.f;
+    bool ok = true;
+    auto convert_v = [&](int jj, float kf) -> bool {
+      const int rv = jj % NRV, vs = jj % NV;
+      if (!mbar_wait_bounded(&rv_full[rv], (jj / NRV) & 1, a.status) || *s_abort) return false;
+      if (jj >= NV && (!mbar_wait_bounded(&v_empty[vs], ((jj / NV) - 1) & 1, a.status) || *s_abort)) return false;
+      const uint8_t* rawv = sRV + rv * Cfg::RV_STAGE;
+      uint8_t* vst = sV + vs * Cfg::V_STAGE;
+      const int kvalid = F - 64 * (p_lo + jj);
+      convert_tile<KV, D, Cfg::V_RB>(rawv, Cfg::RV_CODES, vst, ct, kvalid);
+      if (ct < 64) {
+        float* fac = reinterpret_cast<float*>(vst + Cfg::F16);
+        fac[ct] = kf;
+        fac[64 + ct] = ct < kvalid ? key_factor<KV, D>(rawv + Cfg::RV_CODES, ct) : 0.f;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        q_arrive(&rv_empty[rv]);
+        q_arrive(&v_full[vs]);
+      }
+      return true;
+    };
+    for (int i = 0; ok && i <= n; ++i) {
+      float kf = 0.f;
+      if (i < n) {  // K(i)
+        const int rk = i % NRK, ks = i % NK;
+        ok = mbar_wait_bounded(&rk_full[rk], (i / NRK) & 1, a.status) && !*s_abort;
+        if (ok && i >= NK) ok = mbar_wait_bounded(&k_empty[ks], ((i / NK) - 1) & 1, a.status) && !*s_abort;
+        if (!ok) break;
+        const uint8_t* raw = sRK + rk * Cfg::RK_STAGE;
+        const int kvalid = F - 64 * (p_lo + i);
+        convert_tile<KK, D, Cfg::K_RB>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
+        if (ct < 64 && ct < kvalid) kf = key_factor<KK, D>(raw + Cfg::RK_CODES, ct) * a.scale_log2;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          q_arrive(&rk_empty[rk]);
+          q_arrive(&k_full[ks]);
+        }
+      }
+      if (i >= 1) ok = convert_v(i - 1, kf_prev);
+      kf_prev = kf;
+    }
+    if (!ok) *s_abort = 1;
   } else if (warp == 5) {
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       bool ok = mbar_wait_bounded(q_ready, 0, a.status);
       tc::fence_after();
       for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {
+        if (j < n) {  // S(j) = Q K(j)^T into buffer j & 1
           const int ks = j % NK, sb = j & 1;
-          ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status);
+          ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status) && !*s_abort;
           if (!ok) break;
           tc::fence_after();
-          const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::KV_BYTES), 16, 1024);
+          const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
@@ -316,10 +413,10 @@ __global__ void __launch_bounds__(192, 1)
           tc::commit(&s_full[sb]);
           tc::commit(&k_empty[ks]);
         }
-        if (j >= 1) {
+        if (j >= 1) {  // O += P(j - 1) V(j - 1)
           const int jj = j - 1, vs = jj % NV;
-          ok = mbar_wait_bounded(&v_full[vs], (jj / NV) & 1, a.status);
-          if (ok) ok = mbar_wait_bounded(p_full, jj & 1, a.status);
+          ok = mbar_wait_bounded(&v_full[vs], (jj / NV) & 1, a.status) && !*s_abort;
+          if (ok) ok = mbar_wait_bounded(p_full, jj & 1, a.status) && !*s_abort;
           if (!ok) break;
           tc::fence_after();
           const uint64_t vd = tc::smem_desc(smem_u32(sV + vs * Cfg::V_STAGE), 8192, 1024);
@@ -384,7 +481,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1, vs = j % NV;
       ok = mbar_wait_bounded(&s_full[sb], (j / 2) & 1, a.status) && !*s_abort;
-      // the page's scales travel with its V tile, which stays until PV(j)
+      // the page's factors travel with its V tile, which stays until PV(j)
       if (ok) ok = mbar_wait_bounded(&v_full[vs], (j / NV) & 1, a.status) && !*s_abort;
       if (!ok) break;
       tc::fence_after();
@@ -392,7 +489,7 @@ __global__ void __launch_bounds__(192, 1)
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb, v0);
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb + 32, v1);
       tc::wait_ld();
-      const float* ksc = reinterpret_cast<const float*>(sV + vs * Cfg::V_STAGE + Cfg::KV_BYTES);
+      const float* ksc = reinterpret_cast<const float*>(sV + vs * Cfg::V_STAGE + Cfg::F16);
       const float* vsc = ksc + 64;
       const int kmax = row_valid ? pos - 64 * (p_lo + j) : -1;
       float rmax = -INFINITY;
@@ -474,6 +571,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // ---- teardown: every issued MMA has completed before TMEM is freed ---------
   if (warp < 4 && tid == 0) mbar_wait_bounded(drain, 0, a.status, 200000000ull);
   tc::fence_before();
   __syncthreads();
@@ -482,14 +580,12 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int KK, int KV, int D>
-static cudaError_t launch_passes(const CUtensorMap& tk, const CUtensorMap& tv, const QArgs& a, cudaStream_t s) {
-  using Cfg = QCfg<D>;
-  cudaError_t e = launch_pdl(qdequant_kernel<KK, KV, D>, dim3(a.L, a.H, a.B), dim3(128), 0, s, a);
-  if (e != cudaSuccess) return e;
-  auto k = qprefill_kernel<D>;
+static cudaError_t launch_q(const CUtensorMap& tk, const CUtensorMap& tv, const QArgs& a, cudaStream_t s) {
+  using Cfg = QCfg<KK, KV, D>;
+  auto k = qprefill_kernel<KK, KV, D>;
   static bool attr = false;
   if (!attr) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -498,28 +594,23 @@ static cudaError_t launch_passes(const CUtensorMap& tk, const CUtensorMap& tv, c
 
 template <int KK, int KV>
 static cudaError_t launch_qd(int D, const CUtensorMap& tk, const CUtensorMap& tv, const QArgs& a, cudaStream_t s) {
-  return D == 256   ? launch_passes<KK, KV, 256>(tk, tv, a, s)
-         : D == 128 ? launch_passes<KK, KV, 128>(tk, tv, a, s)
-                    : launch_passes<KK, KV, 64>(tk, tv, a, s);
+  return D == 256   ? launch_q<KK, KV, 256>(tk, tv, a, s)
+         : D == 128 ? launch_q<KK, KV, 128>(tk, tv, a, s)
+                    : launch_q<KK, KV, 64>(tk, tv, a, s);
 }
 
-size_t qprefill_workspace_bytes(const nk_pool* p, int B) {
-  if (p->desc.profile == NK_BF16) return 0;
-  return QScratch::bytes(B, p->desc.num_kv_heads, p->L, p->desc.head_dim);
-}
-
-// Quantized-pool prefill: dequant pass + tensor pass.  The caller
-// (nk_paged_prefill_attention) has checked shapes, pointers and alignment.
+// Quantized-pool prefill.  The caller (nk_paged_prefill_attention) has checked
+// shapes, pointers and alignment; the workspace holds only the split partials.
 int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* tables, const int32_t* table_rows,
                     const int32_t* prefix_len, const int32_t* chunk_len, int B, int Tc, int Hq, float scale_log2,
                     void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t s) {
   const int D = p->desc.head_dim, H = p->desc.num_kv_heads;
   const int tiles = (Tc + 128 / (Hq / H) - 1) / (128 / (Hq / H));
   const int nsplit = prefill_nsplit(tiles * H * B, p->num_sms);
-  const size_t scr = (QScratch::bytes(B, H, p->L, D) + 255) / 256 * 256;
-  const size_t need = scr + prefill_split_bytes(B, H, tiles, nsplit, D);
-  if (!ws || ws_bytes < need) return fail(NK_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
-  if (!aligned16(ws)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const size_t need = prefill_split_bytes(B, H, tiles, nsplit, D);
+  if (need && (!ws || ws_bytes < need))
+    return fail(NK_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
+  if (need && !aligned16(ws)) return fail(NK_ERR_ALIGN, "workspace must be 16-byte aligned");
   QArgs a;
   const int np = p->n_planes;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -527,11 +618,8 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   a.table_rows = table_rows;
   a.prefix_len = prefix_len;
   a.chunk_len = chunk_len;
-  a.kc = static_cast<const uint8_t*>(p->ptrs[layer * np + 0]);
-  a.vc = static_cast<const uint8_t*>(p->ptrs[layer * np + 1]);
   a.ks = static_cast<const uint8_t*>(p->ptrs[layer * np + 2]);
   a.vs = static_cast<const uint8_t*>(p->ptrs[layer * np + 3]);
-  a.scr = QScratch::at(ws, B, H, p->L, D);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.status = p->status;
@@ -545,14 +633,10 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   a.L = p->L;
   a.M = p->M;
   a.C = p->desc.max_concurrency;
-  a.sp = prefill_split_at(static_cast<char*>(ws) + scr, B, H, tiles, nsplit);
+  a.sp = prefill_split_at(ws, B, H, tiles, nsplit);
   a.head_major = p->desc.order == NK_HEAD_MAJOR;
-  const int64_t rows = static_cast<int64_t>(B) * H * p->L * 64;
-  CUtensorMap tk, tv;
-  int rc = encode_code_tmap(&tk, a.scr.k, D * 2, rows);
-  if (rc) return rc;
-  rc = encode_code_tmap(&tv, a.scr.v, D * 2, rows);
-  if (rc) return rc;
+  const CUtensorMap& tk = p->tmap[layer * 2 + 0];
+  const CUtensorMap& tv = p->tmap[layer * 2 + 1];
   cudaError_t e;
   switch (p->desc.profile) {
     case NK_INT8_G64: e = launch_qd<KIND_INT8, KIND_INT8>(D, tk, tv, a, s); break;

@@ -341,7 +341,7 @@ class Pool:
             lse = torch.full((B, Tc, Hq), float("-inf"), dtype=torch.float32, device=q.device)
         n = nk_prefill_workspace_bytes(self.handle, B, Tc, Hq)
         ws = workspace
-        if ws is None and n:   # dequant scratch and split partials, zero-filled once, kept for reuse
+        if ws is None and n:   # split partials and counters, zero-filled once, kept for reuse
             if getattr(self, "_pws", None) is None or self._pws.numel() < n:
                 self._pws = torch.zeros(n, dtype=torch.uint8, device=q.device)
             ws = self._pws

@@ -201,3 +201,18 @@ def test_prefill_head_major_plane_order(profile):
     w = prefill_workload(2, 8, 256, 1024, prefixes=[133, 0], chunks=[300, 77], Tc=320, seed=29,
                          profile=profile)
     run_prefill(w, order="head_major")
+
+
+@pytest.mark.parametrize("profile", ["bf16", "int8_g64", "fp8_row", "nvfp4_g16", "k8v4"])
+def test_prefill_workspace_does_not_grow_with_the_context(profile):
+    """The pages are dequantized inside the attention kernel, so the prefill
+    workspace (split partials only) is the same for a 4096-token pool and a
+    131072-token pool of the same heads, rows and chunk."""
+    from paged_kv_cache_append_gb300 import nk
+    sizes = []
+    for S in (4096, 131072):
+        L = S // 64
+        pool = nk.Pool(profile, 1, 2, 256, S, 2, L)
+        sizes.append(nk.nk_prefill_workspace_bytes(pool.handle, 2, 2048, 16))
+        pool.close()
+    assert sizes[0] == sizes[1], sizes

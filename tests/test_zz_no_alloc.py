@@ -7,10 +7,12 @@ nk_paged_decode_attention_noalloc serves them: it keeps the split-K partials
 in a static device array of the library instead of a caller workspace.
 
 These tests call it through the C ABI twice in a row (the array keeps the
-previous call's contents) and check each result against what
-nk_paged_decode_attention returns for the same inputs and against the oracle,
-both within the parity tolerance of the other tests.  The shapes cover a
-plan that fits the array, plans whose split count must be lowered to fit
+previous call's contents) and check each result against the oracle and
+against what nk_paged_decode_attention returns for the same inputs, within
+the parity tolerance of the other tests (against the other entry point,
+whose output is itself bf16-rounded, half an ulp per side).  The shapes
+cover a plan that fits the array, plans whose split count must be lowered to
+fit
 (with at least one split per row, with fewer slots than rows, and with the
 tcgen05 kernel that takes several pieces per CTA), and a call too large for
 the array, which is rejected before any launch.
@@ -95,8 +97,10 @@ def _run(w, full_oracle=True, oracle_rows=None, lowered=False):
         out, lse = _noalloc(lib, sc, q, rows, fr, w)
         torch.cuda.synchronize()
         out, lse = out.cpu(), lse.cpu()
-        compare_attention(out, lse, ref_out, ref_lse)          # the workspace entry point
         compare_attention(out[check], lse[check], orc_out, orc_lse)   # the oracle
+        # the workspace entry point: both outputs are bf16-rounded, so they
+        # may differ by a full ulp (half from each side) beyond 2e-2
+        compare_attention(out, lse, ref_out, ref_lse, ref_rounded=True)
 
 
 def test_noalloc_plan_fits_the_scratch():
