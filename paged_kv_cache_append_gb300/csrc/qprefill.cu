@@ -13,9 +13,10 @@
 //               scale tile (bulk copy) into a raw K ring and a raw V ring;
 //   warps 6-9   converters: each page's codes become an f16 tile in the
 //               layout the MMAs read (rows = keys, 128-byte rows of 64 dims,
-//               128-byte swizzle), K one page ahead of V; with the V tile
-//               they store each key's fp32 factors (K: score factor times
-//               softmax_scale * log2 e; V: softmax weight factor);
+//               128-byte swizzle), K one page ahead of V; with K they
+//               store each key's fp32 factors (K: score factor times
+//               softmax_scale * log2 e; V: softmax weight factor) in a
+//               small ring of their own;
 //   warp 5      MMA issuer: S = Q K^T (A = Q in TMEM, B = the f16 K tile),
 //               O += P V (A = P in TMEM, B = the f16 V tile, MN-major);
 //   warps 0-3   Q to TMEM (f16, each query row prescaled by a power of two),
@@ -75,17 +76,21 @@ struct QArgs {
 };
 
 // INT8-G64 keys: the power of two e (0..7) with 127 * max_g s_g * 2^-e < 2^15
-// (or the largest, 7, when binary16's range forbids it).
+// (or the largest, 7, when binary16's range forbids it).  The scales are
+// finite and >= 0, so 127 * max_g s_g is 0 or a normal fp32 x, and
+// x < 2^ex for ex = (biased exponent of x) - 126.
 template <int D>
 __device__ __forceinline__ int int8_row_shift(const uint8_t* scale_row) {
   float smax = 0.f;
 #pragma unroll
   for (int g = 0; g < D / 64; ++g)
     smax = fmaxf(smax, fabsf(__half2float(*reinterpret_cast<const __half*>(scale_row + 2 * g))));
-  int ex = 0;
-  frexpf(127.f * smax, &ex);  // 127 * smax < 2^ex
+  const int ex = static_cast<int>((__float_as_uint(127.f * smax) >> 23) & 0xFFu) - 126;
   return min(max(ex - 15, 0), 7);
 }
+
+// 2^-e for e in [0, 7] (a normal fp32).
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
 template <int KK, int KV, int D>
 struct QCfg {
@@ -96,24 +101,31 @@ struct QCfg {
   static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
   static constexpr int F16 = 64 * D * 2;                           // one f16 page tile
   static constexpr int K_STAGE = F16;
-  static constexpr int V_STAGE = F16 + 1024;                       // + 128 fp32 factors per key
+  static constexpr int V_STAGE = F16;
+  static constexpr int NF = 4;                                     // factor ring (512 B per page)
   static constexpr int RK_CODES = (64 * KCB + 1023) / 1024 * 1024;  // raw K code tile (1024-aligned)
   static constexpr int RV_CODES = (64 * VCB + 1023) / 1024 * 1024;
   static constexpr int RK_STAGE = (RK_CODES + 64 * KSB + 1023) / 1024 * 1024;
   static constexpr int RV_STAGE = (RV_CODES + 64 * VSB + 1023) / 1024 * 1024;
-  static constexpr int NK = D == 256 ? 2 : D == 128 ? 4 : 6;  // f16 K ring
-  static constexpr int NV = NK;                                // f16 V ring
-  static constexpr int NRK = D == 256 ? (RK_STAGE <= 10240 ? 3 : 2) : 4;  // raw rings
-  static constexpr int NRV = D == 256 ? (RV_STAGE <= 10240 ? 3 : 2) : 4;
+  // FP8-row keys with 128-byte code rows (head_dim >= 128, the swizzle of the
+  // f16 tiles) go to the tensor cores as raw E4M3 codes (kind::f8f6f4), with
+  // q split exactly into two E4M3 terms: no K conversion, no f16 K tile.
+  static constexpr bool K8MMA = (KK == KIND_FP8) && D >= 128;
+  static constexpr int NK = K8MMA ? 0 : D == 256 ? 2 : D == 128 ? 4 : 6;  // f16 K ring
+  static constexpr int NV = K8MMA ? (D == 256 ? 3 : 4) : NK;              // f16 V ring
+  static constexpr int NRK = K8MMA ? (D == 256 ? 3 : 6) : D == 256 ? (RK_STAGE <= 10240 ? 3 : 2) : 4;  // raw rings
+  static constexpr int NRV = D == 256 ? (RV_STAGE <= 10240 || K8MMA ? 3 : 2) : 4;
+  static constexpr int NKF = K8MMA ? NRK : NK;  // K ready barriers: per raw slot (K8MMA) or f16 slot
   static constexpr int OFF_V = NK * K_STAGE;
   static constexpr int OFF_RK = OFF_V + NV * V_STAGE;
   static constexpr int OFF_RV = OFF_RK + NRK * RK_STAGE;
-  static constexpr int OFF_BAR = OFF_RV + NRV * RV_STAGE;
-  static constexpr int NBAR = 2 * NK + 2 * NV + 2 * NRK + 2 * NRV + 2 + 4;
+  static constexpr int OFF_F = OFF_RV + NRV * RV_STAGE;
+  static constexpr int OFF_BAR = OFF_F + NF * 512;
+  static constexpr int NBAR = 2 * NKF + 2 * NV + 2 * NRK + 2 * NRV + 2 * NF + 2 + 4;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 64 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0, COL_Q = 128, COL_O = 256;
-  static constexpr uint32_t ID_S = tc::idesc_f16(128, 64, false, false);
+  static constexpr uint32_t ID_S = K8MMA ? tc::idesc_e4m3(128, 64) : tc::idesc_f16(128, 64, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
   static constexpr int UNITS = 64 * (D / 16);  // (key, 16-dim group) units of a tile
   static constexpr int UPT = UNITS / (32 * NCONV);  // units per converter thread
@@ -181,7 +193,7 @@ template <int KIND, int D>
 __device__ __forceinline__ float key_factor(const uint8_t* scales, int r) {
   constexpr int SB = scale_row_bytes<KIND>(D);
   if constexpr (KIND == KIND_FP8) return __half2float(*reinterpret_cast<const __half*>(scales + r * SB));
-  else if constexpr (KIND == KIND_INT8) return ldexpf(1.f, int8_row_shift<D>(scales + r * SB));
+  else if constexpr (KIND == KIND_INT8) return __uint_as_float(static_cast<uint32_t>(127 + int8_row_shift<D>(scales + r * SB)) << 23);
   else return 1.f;
 }
 
@@ -205,7 +217,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
 #pragma unroll
   for (int k = 0; k < UPT; ++k) {
     float shift = 1.f;
-    if constexpr (KIND == KIND_INT8) shift = ldexpf(1.f, -int8_row_shift<D>(scales + rr[k] * SB));
+    if constexpr (KIND == KIND_INT8) shift = pow2_neg(int8_row_shift<D>(scales + rr[k] * SB));
     convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
   }
 #pragma unroll
@@ -220,23 +232,27 @@ template <int KK, int KV, int D>
 __global__ void __launch_bounds__(320, 1)
     qprefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, QArgs a) {
   using Cfg = QCfg<KK, KV, D>;
-  constexpr int NK = Cfg::NK, NV = Cfg::NV, NRK = Cfg::NRK, NRV = Cfg::NRV;
+  constexpr int NK = Cfg::NK, NV = Cfg::NV, NRK = Cfg::NRK, NRV = Cfg::NRV, NF = Cfg::NF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::OFF_V;
   uint8_t* sRK = smem + Cfg::OFF_RK;
   uint8_t* sRV = smem + Cfg::OFF_RV;
+  float* sF = reinterpret_cast<float*>(smem + Cfg::OFF_F);  // [NF][128]: 64 K factors, 64 V factors
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  uint64_t* k_full = bars;             // f16 K tile ready (converters)
-  uint64_t* k_empty = k_full + NK;     // S of the tile done (MMA commit)
-  uint64_t* v_full = k_empty + NK;     // f16 V tile + factors ready (converters)
+  constexpr int NKF = Cfg::NKF;
+  uint64_t* k_full = bars;             // K tile ready for the MMA (converters)
+  uint64_t* k_empty = k_full + NKF;    // S of the f16 tile done (MMA commit; f16 K only)
+  uint64_t* v_full = k_empty + NKF;    // f16 V tile ready (converters)
   uint64_t* v_empty = v_full + NV;     // PV of the tile done (MMA commit)
   uint64_t* rk_full = v_empty + NV;    // raw K tile landed (TMA)
   uint64_t* rk_empty = rk_full + NRK;  // raw K tile converted
   uint64_t* rv_full = rk_empty + NRK;
   uint64_t* rv_empty = rv_full + NRV;
-  uint64_t* s_full = rv_empty + NRV;  // [2]
+  uint64_t* f_full = rv_empty + NRV;  // factors of a page written (converters)
+  uint64_t* f_empty = f_full + NF;    // factors read (softmax warps)
+  uint64_t* s_full = f_empty + NF;    // [2]
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 1;
   uint64_t* q_ready = o_done + 1;
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(320, 1)
   const int32_t* table = a.tables + static_cast<int64_t>(row) * a.L + p_lo;
 
   if (tid == 0) {
-    for (int i = 0; i < NK; ++i) {
+    for (int i = 0; i < NKF; ++i) {
       mbar_init(&k_full[i], Cfg::NCONV);
       mbar_init(&k_empty[i], 1);
     }
@@ -281,11 +297,15 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < NRK; ++i) {
       mbar_init(&rk_full[i], 1);
-      mbar_init(&rk_empty[i], Cfg::NCONV);
+      mbar_init(&rk_empty[i], Cfg::K8MMA ? 1 : Cfg::NCONV);  // MMA commit, or the converters
     }
     for (int i = 0; i < NRV; ++i) {
       mbar_init(&rv_full[i], 1);
       mbar_init(&rv_empty[i], Cfg::NCONV);
+    }
+    for (int i = 0; i < NF; ++i) {
+      mbar_init(&f_full[i], Cfg::NCONV);
+      mbar_init(&f_empty[i], 4);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
@@ -346,52 +366,64 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp >= 6) {
     // ------------- converters: K one page ahead of V ------------------------------
     // Order K(0), K(1), V(0), K(2), V(1), ...: the MMA issues S(i) before
-    // PV(i - 1).  Thread ct < 64 carries key ct's K factor from K(i) to the
-    // factor slot of V(i), which is written with the V tile.
+    // PV(i - 1).  With K(i) the converters also write page i's per-key
+    // factors (K from the K scales, V from the V scales, whose raw tile was
+    // loaded with the K tile) into the factor ring, so the softmax of a page
+    // never waits for its V tile.
     const int ct = tid - 192;  // 0..127
-    float kf_prev = 0.f;
     bool ok = true;
-    auto convert_v = [&](int jj, float kf) -> bool {
-      const int rv = jj % NRV, vs = jj % NV;
-      if (!mbar_wait_bounded(&rv_full[rv], (jj / NRV) & 1, a.status) || *s_abort) return false;
-      if (jj >= NV && (!mbar_wait_bounded(&v_empty[vs], ((jj / NV) - 1) & 1, a.status) || *s_abort)) return false;
-      const uint8_t* rawv = sRV + rv * Cfg::RV_STAGE;
-      uint8_t* vst = sV + vs * Cfg::V_STAGE;
-      const int kvalid = F - 64 * (p_lo + jj);
-      convert_tile<KV, D, Cfg::V_RB>(rawv, Cfg::RV_CODES, vst, ct, kvalid);
-      if (ct < 64) {
-        float* fac = reinterpret_cast<float*>(vst + Cfg::F16);
-        fac[ct] = kf;
-        fac[64 + ct] = ct < kvalid ? key_factor<KV, D>(rawv + Cfg::RV_CODES, ct) : 0.f;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        q_arrive(&rv_empty[rv]);
-        q_arrive(&v_full[vs]);
-      }
-      return true;
-    };
     for (int i = 0; ok && i <= n; ++i) {
-      float kf = 0.f;
-      if (i < n) {  // K(i)
-        const int rk = i % NRK, ks = i % NK;
+      if (i < n) {  // K(i) and the factors of page i
+        const int rk = i % NRK, rv = i % NRV, fs = i % NF;
         ok = mbar_wait_bounded(&rk_full[rk], (i / NRK) & 1, a.status) && !*s_abort;
-        if (ok && i >= NK) ok = mbar_wait_bounded(&k_empty[ks], ((i / NK) - 1) & 1, a.status) && !*s_abort;
         if (!ok) break;
         const uint8_t* raw = sRK + rk * Cfg::RK_STAGE;
         const int kvalid = F - 64 * (p_lo + i);
-        convert_tile<KK, D, Cfg::K_RB>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
-        if (ct < 64 && ct < kvalid) kf = key_factor<KK, D>(raw + Cfg::RK_CODES, ct) * a.scale_log2;
+        const bool live = ct < 64 && ct < kvalid;
+        // key ct's K factor, read before the raw slot can be released
+        const float kf = live ? key_factor<KK, D>(raw + Cfg::RK_CODES, ct) * a.scale_log2 : 0.f;
+        if constexpr (!Cfg::K8MMA) {
+          const int ks = i % NK;
+          if (i >= NK) ok = mbar_wait_bounded(&k_empty[ks], ((i / NK) - 1) & 1, a.status) && !*s_abort;
+          if (!ok) break;
+          convert_tile<KK, D, Cfg::K_RB>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            q_arrive(&rk_empty[rk]);
+            q_arrive(&k_full[ks]);
+          }
+        }
+        ok = mbar_wait_bounded(&rv_full[rv], (i / NRV) & 1, a.status) && !*s_abort;
+        if (ok && i >= NF) ok = mbar_wait_bounded(&f_empty[fs], ((i / NF) - 1) & 1, a.status) && !*s_abort;
+        if (!ok) break;
+        if (ct < 64) {
+          float* fac = sF + fs * 128;
+          fac[ct] = kf;
+          fac[64 + ct] = live ? key_factor<KV, D>(sRV + rv * Cfg::RV_STAGE + Cfg::RV_CODES, ct) : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          q_arrive(&f_full[fs]);
+          // the raw E4M3 tile is the MMA operand itself; the K scales have
+          // been read, so the MMA may release the slot after S(i)
+          if constexpr (Cfg::K8MMA) q_arrive(&k_full[rk]);
+        }
+      }
+      if (i >= 1) {  // V(i - 1)
+        const int jj = i - 1, rv = jj % NRV, vs = jj % NV;
+        ok = mbar_wait_bounded(&rv_full[rv], (jj / NRV) & 1, a.status) && !*s_abort;
+        if (ok && jj >= NV) ok = mbar_wait_bounded(&v_empty[vs], ((jj / NV) - 1) & 1, a.status) && !*s_abort;
+        if (!ok) break;
+        convert_tile<KV, D, Cfg::V_RB>(sRV + rv * Cfg::RV_STAGE, Cfg::RV_CODES, sV + vs * Cfg::V_STAGE, ct,
+                                       F - 64 * (p_lo + jj));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          q_arrive(&rk_empty[rk]);
-          q_arrive(&k_full[ks]);
+          q_arrive(&rv_empty[rv]);
+          q_arrive(&v_full[vs]);
         }
       }
-      if (i >= 1) ok = convert_v(i - 1, kf_prev);
-      kf_prev = kf;
     }
     if (!ok) *s_abort = 1;
   } else if (warp == 5) {
@@ -401,17 +433,38 @@ __global__ void __launch_bounds__(320, 1)
       tc::fence_after();
       for (int j = 0; ok && j <= n; ++j) {
         if (j < n) {  // S(j) = Q K(j)^T into buffer j & 1
-          const int ks = j % NK, sb = j & 1;
-          ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status) && !*s_abort;
-          if (!ok) break;
-          tc::fence_after();
-          const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE), 16, 1024);
+          const int sb = j & 1;
+          if constexpr (Cfg::K8MMA) {
+            // E4M3 codes (32 per instruction: 32 bytes of a 128-byte row, as
+            // 16 f16 values are), q_hi in columns [COL_Q, COL_Q + D/4), q_lo
+            // in the next D/4
+            const int rk = j % NRK;
+            ok = mbar_wait_bounded(&k_full[rk], (j / NRK) & 1, a.status) && !*s_abort;
+            if (!ok) break;
+            tc::fence_after();
+            const uint64_t kd = tc::smem_desc(smem_u32(sRK + rk * Cfg::RK_STAGE), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
-                       kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
-          tc::commit(&s_full[sb]);
-          tc::commit(&k_empty[ks]);
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int kk = 0; kk < D / 32; ++kk)
+                tc::mma_ts_f8(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + part * (D / 4) + kk * 8,
+                              kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S,
+                              part > 0 || kk > 0);
+            tc::commit(&s_full[sb]);
+            tc::commit(&rk_empty[rk]);
+          } else {
+            const int ks = j % NK;
+            ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status) && !*s_abort;
+            if (!ok) break;
+            tc::fence_after();
+            const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
+                         kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
+            tc::commit(&s_full[sb]);
+            tc::commit(&k_empty[ks]);
+          }
         }
         if (j >= 1) {  // O += P(j - 1) V(j - 1)
           const int jj = j - 1, vs = jj % NV;
@@ -453,23 +506,59 @@ __global__ void __launch_bounds__(320, 1)
         }
       int ex = 0;
       if (mx > 0.f) frexpf(mx, &ex);
-      const int e = mx > 0.f ? min(15 - ex, 100) : 0;  // 2^e stays finite in fp32
+      // f16 q: max|q| 2^e in [2^14, 2^15); E4M3 q: max|q| 2^e in [2^7, 2^8)
+      const int e = mx > 0.f ? min((Cfg::K8MMA ? 8 : 15) - ex, 100) : 0;  // 2^e stays finite in fp32
       const float qf = ldexpf(1.f, e);
       rs = ldexpf(1.f, -e);
+      if constexpr (Cfg::K8MMA) {
+        // q' = q 2^e = hi + lo with hi = E4M3(q') and lo = E4M3(q' - hi), both
+        // round to nearest even.  Where |q'| >= 2^-2 the residual is an exact
+        // E4M3 value (q' has 8 significant bits, hi keeps 4, the rest fit
+        // 4 more within E4M3's range), so hi + lo = q'; smaller elements are
+        // kept to 2^-10 absolute, i.e. 2^-17 max|q'|.  A 32-bit column holds
+        // 4 consecutive dims, the lowest in its low byte.
 #pragma unroll 1
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t qv[32];
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t hv[16], lv[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = row_valid ? src[c0 / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = row_valid ? src[c0 / 8 + u] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t hpair[4], lpair[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-            qv[4 * u + k] = pack_f16x2(__low2float(v) * qf, __high2float(v) * qf);
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+              const float x0 = __low2float(v) * qf, x1 = __high2float(v) * qf;
+              const uint16_t h2 = f32x2_to_e4m3x2(x0, x1);
+              const uint32_t hb32 = e4m3x2_to_f16x2(h2);
+              const __half2 hb = *reinterpret_cast<const __half2*>(&hb32);
+              hpair[k] = h2;
+              lpair[k] = f32x2_to_e4m3x2(x0 - __low2float(hb), x1 - __high2float(hb));
+            }
+            hv[2 * u] = hpair[0] | (hpair[1] << 16);
+            hv[2 * u + 1] = hpair[2] | (hpair[3] << 16);
+            lv[2 * u] = lpair[0] | (lpair[1] << 16);
+            lv[2 * u + 1] = lpair[2] | (lpair[3] << 16);
           }
+          tc::st16(tmem + lane_base + Cfg::COL_Q + c0 / 4, hv);
+          tc::st16(tmem + lane_base + Cfg::COL_Q + D / 4 + c0 / 4, lv);
         }
-        tc::st32(tmem + lane_base + Cfg::COL_Q + c0, qv);
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = row_valid ? src[c0 / 4 + u] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+              qv[4 * u + k] = pack_f16x2(__low2float(v) * qf, __high2float(v) * qf);
+            }
+          }
+          tc::st32(tmem + lane_base + Cfg::COL_Q + c0, qv);
+        }
       }
       tc::wait_st();
       tc::fence_before();
@@ -479,17 +568,16 @@ __global__ void __launch_bounds__(320, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int sb = j & 1, vs = j % NV;
+      const int sb = j & 1, fs = j % NF;
       ok = mbar_wait_bounded(&s_full[sb], (j / 2) & 1, a.status) && !*s_abort;
-      // the page's factors travel with its V tile, which stays until PV(j)
-      if (ok) ok = mbar_wait_bounded(&v_full[vs], (j / NV) & 1, a.status) && !*s_abort;
+      if (ok) ok = mbar_wait_bounded(&f_full[fs], (j / NF) & 1, a.status) && !*s_abort;
       if (!ok) break;
       tc::fence_after();
       uint32_t v0[32], v1[32];
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb, v0);
       tc::ld32(tmem + lane_base + Cfg::COL_S + 64 * sb + 32, v1);
       tc::wait_ld();
-      const float* ksc = reinterpret_cast<const float*>(sV + vs * Cfg::V_STAGE + Cfg::F16);
+      const float* ksc = sF + fs * 128;
       const float* vsc = ksc + 64;
       const int kmax = row_valid ? pos - 64 * (p_lo + j) : -1;
       float rmax = -INFINITY;
@@ -537,6 +625,8 @@ __global__ void __launch_bounds__(320, 1)
         pk[16 + 2 * c4] = pack_f16x2(p1[0] * sbv[0], p1[1] * sbv[1]);
         pk[16 + 2 * c4 + 1] = pack_f16x2(p1[2] * sbv[2], p1[3] * sbv[3]);
       }
+      __syncwarp();
+      if (lane == 0) q_arrive(&f_empty[fs]);  // this warp is done with the page's factors
       l = l * factor + sum;
       if (j >= 1) {
         ok = mbar_wait_bounded(o_done, (j - 1) & 1, a.status) && !*s_abort;
