@@ -94,8 +94,10 @@ __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static
 
 template <int KK, int KV, int D>
 struct QCfg {
-  static constexpr int THREADS = 320;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-9 converters
-  static constexpr int NCONV = 4;      // converter warps
+  // converter warps (6 .. 5 + NCONV): 8 where K and V are both converted, 4
+  // where only V is (the raw FP8 keys go to the tensor cores)
+  static constexpr int NCONV = (KK == KIND_FP8 && D >= 128) ? 4 : 8;
+  static constexpr int THREADS = 192 + 32 * NCONV;  // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
   static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
   static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
@@ -115,7 +117,7 @@ struct QCfg {
   static constexpr int NV = K8MMA ? (D == 256 ? 3 : 4) : NK;              // f16 V ring
   static constexpr int NRK = K8MMA ? (D == 256 ? 3 : 6) : D == 256 ? (RK_STAGE <= 10240 ? 3 : 2) : 4;  // raw rings
   static constexpr int NRV = D == 256 ? (RV_STAGE <= 10240 || K8MMA ? 3 : 2) : 4;
-  static constexpr int NKF = K8MMA ? NRK : NK;  // K ready barriers: per raw slot (K8MMA) or f16 slot
+  static constexpr int NKF = K8MMA ? 0 : NK;  // f16 K ready barriers (the raw FP8 keys need none)
   static constexpr int OFF_V = NK * K_STAGE;
   static constexpr int OFF_RK = OFF_V + NV * V_STAGE;
   static constexpr int OFF_RV = OFF_RK + NRK * RK_STAGE;
@@ -128,8 +130,6 @@ struct QCfg {
   static constexpr uint32_t ID_S = K8MMA ? tc::idesc_e4m3(128, 64) : tc::idesc_f16(128, 64, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
   static constexpr int UNITS = 64 * (D / 16);  // (key, 16-dim group) units of a tile
-  static constexpr int UPT = UNITS / (32 * NCONV);  // units per converter thread
-  static_assert(UPT * 32 * NCONV == UNITS, "converter units");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -167,13 +167,19 @@ __device__ __forceinline__ void convert16(const uint8_t* codes, const uint8_t* s
                     e4m3x2_to_f16x2(static_cast<uint16_t>(w.w & 0xFFFFu)),
                     e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
   } else if constexpr (KIND == KIND_INT8) {
+    // binary16 code times the binary16 scale s_g 2^-e (exact unless the shift
+    // takes it below binary16's normal range), the product rounded once
     const uint4 w = *reinterpret_cast<const uint4*>(codes + raw_off<RB>(r, 16 * g));
-    const float sg = __half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * g) / 64))) * shift;
-    const int8_t* c = reinterpret_cast<const int8_t*>(&w);
+    const __half s16 = __float2half_rn(
+        __half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * g) / 64))) * shift);
+    const uint32_t s2 = pack_h2(s16, s16);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
     uint32_t h[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      h[i] = pack_f16x2(static_cast<float>(c[2 * i]) * sg, static_cast<float>(c[2 * i + 1]) * sg);
+    for (int q = 0; q < 4; ++q) {
+      h[2 * q] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x1100)), s2);
+      h[2 * q + 1] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x3322)), s2);
+    }
     lo = make_uint4(h[0], h[1], h[2], h[3]);
     hi = make_uint4(h[4], h[5], h[6], h[7]);
   } else {  // NVFP4: 8 bytes of codes times the group's E4M3 scale
@@ -197,29 +203,34 @@ __device__ __forceinline__ float key_factor(const uint8_t* scales, int r) {
   else return 1.f;
 }
 
-// One converter thread's share of a page tile: units (key r, 16-dim group g)
-// u = ct + 128 k; keys at or past `kvalid` become zeros.
-template <int KIND, int D, int RB>
+// One converter thread's share of a page tile, in units of (key r, 16-dim
+// group g): key r = (ct & 7) + 8 ((ct >> 3) & 7) and the UPT groups
+// UPT (ct >> 6) + [0, UPT), so every unit of a thread shares its key (the
+// INT8 key shift is computed once).  Eight consecutive threads take eight
+// consecutive keys of one group, so the swizzled 16-byte loads and stores are
+// free of bank conflicts; the next eight threads take their groups one step
+// ahead, which keeps the 8-byte NVFP4 loads (16 threads per access) apart.
+// NCT, the number of converter threads, is a multiple of 64; keys at or past
+// `kvalid` become zeros.
+template <int KIND, int D, int RB, int NCT>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, uint8_t* f16, int ct, int kvalid) {
-  constexpr int GPR = D / 16;  // 16-dim groups per key
-  constexpr int UPT = (64 * GPR) / 128;
+  constexpr int GPR = D / 16;            // 16-dim groups per key
+  constexpr int UPT = (64 * GPR) / NCT;  // units per thread
+  static_assert(UPT * NCT == 64 * GPR && UPT >= 1, "converter units");
   constexpr int SB = scale_row_bytes<KIND>(D);
   const uint8_t* scales = raw + raw_codes;
-  uint4 lo[UPT], hi[UPT];
   int rr[UPT], gg[UPT];
 #pragma unroll
   for (int k = 0; k < UPT; ++k) {
-    const int u = ct + 128 * k;
-    rr[k] = (u & 7) + 8 * ((u >> 3) / GPR);
-    gg[k] = (u >> 3) % GPR;
+    rr[k] = (ct & 7) + 8 * ((ct >> 3) & 7);
+    gg[k] = UPT * (ct >> 6) + (k + ((ct >> 3) & 1)) % UPT;
   }
+  float shift = 1.f;
+  if constexpr (KIND == KIND_INT8) shift = pow2_neg(int8_row_shift<D>(scales + rr[0] * SB));
+  uint4 lo[UPT], hi[UPT];
   // every raw load of the thread before any store (the stores could alias)
 #pragma unroll
-  for (int k = 0; k < UPT; ++k) {
-    float shift = 1.f;
-    if constexpr (KIND == KIND_INT8) shift = pow2_neg(int8_row_shift<D>(scales + rr[k] * SB));
-    convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
-  }
+  for (int k = 0; k < UPT; ++k) convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
 #pragma unroll
   for (int k = 0; k < UPT; ++k) {
     if (rr[k] >= kvalid) lo[k] = hi[k] = make_uint4(0u, 0u, 0u, 0u);
@@ -229,7 +240,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
 }
 
 template <int KK, int KV, int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
     qprefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, QArgs a) {
   using Cfg = QCfg<KK, KV, D>;
   constexpr int NK = Cfg::NK, NV = Cfg::NV, NRK = Cfg::NRK, NRV = Cfg::NRV, NF = Cfg::NF;
@@ -242,12 +253,12 @@ __global__ void __launch_bounds__(320, 1)
   float* sF = reinterpret_cast<float*>(smem + Cfg::OFF_F);  // [NF][128]: 64 K factors, 64 V factors
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   constexpr int NKF = Cfg::NKF;
-  uint64_t* k_full = bars;             // K tile ready for the MMA (converters)
+  uint64_t* k_full = bars;             // f16 K tile ready for the MMA (converters)
   uint64_t* k_empty = k_full + NKF;    // S of the f16 tile done (MMA commit; f16 K only)
   uint64_t* v_full = k_empty + NKF;    // f16 V tile ready (converters)
   uint64_t* v_empty = v_full + NV;     // PV of the tile done (MMA commit)
   uint64_t* rk_full = v_empty + NV;    // raw K tile landed (TMA)
-  uint64_t* rk_empty = rk_full + NRK;  // raw K tile converted
+  uint64_t* rk_empty = rk_full + NRK;  // raw K tile consumed
   uint64_t* rv_full = rk_empty + NRK;
   uint64_t* rv_empty = rv_full + NRV;
   uint64_t* f_full = rv_empty + NRV;  // factors of a page written (converters)
@@ -297,7 +308,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < NRK; ++i) {
       mbar_init(&rk_full[i], 1);
-      mbar_init(&rk_empty[i], Cfg::K8MMA ? 1 : Cfg::NCONV);  // MMA commit, or the converters
+      // released by the converters; with raw FP8 keys also by the MMA commit
+      mbar_init(&rk_empty[i], Cfg::K8MMA ? 1 + Cfg::NCONV : Cfg::NCONV);
     }
     for (int i = 0; i < NRV; ++i) {
       mbar_init(&rv_full[i], 1);
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(320, 1)
     // factors (K from the K scales, V from the V scales, whose raw tile was
     // loaded with the K tile) into the factor ring, so the softmax of a page
     // never waits for its V tile.
-    const int ct = tid - 192;  // 0..127
+    const int ct = tid - 192;  // 0 .. 32 NCONV - 1
     bool ok = true;
     for (int i = 0; ok && i <= n; ++i) {
       if (i < n) {  // K(i) and the factors of page i
@@ -386,7 +398,7 @@ __global__ void __launch_bounds__(320, 1)
           const int ks = i % NK;
           if (i >= NK) ok = mbar_wait_bounded(&k_empty[ks], ((i / NK) - 1) & 1, a.status) && !*s_abort;
           if (!ok) break;
-          convert_tile<KK, D, Cfg::K_RB>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
+          convert_tile<KK, D, Cfg::K_RB, 32 * Cfg::NCONV>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
@@ -405,9 +417,9 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         if (lane == 0) {
           q_arrive(&f_full[fs]);
-          // the raw E4M3 tile is the MMA operand itself; the K scales have
-          // been read, so the MMA may release the slot after S(i)
-          if constexpr (Cfg::K8MMA) q_arrive(&k_full[rk]);
+          // the raw E4M3 tile is the MMA operand itself: the slot is free once
+          // these scale reads and S(i) (the MMA's commit) are both done
+          if constexpr (Cfg::K8MMA) q_arrive(&rk_empty[rk]);
         }
       }
       if (i >= 1) {  // V(i - 1)
@@ -415,7 +427,7 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait_bounded(&rv_full[rv], (jj / NRV) & 1, a.status) && !*s_abort;
         if (ok && jj >= NV) ok = mbar_wait_bounded(&v_empty[vs], ((jj / NV) - 1) & 1, a.status) && !*s_abort;
         if (!ok) break;
-        convert_tile<KV, D, Cfg::V_RB>(sRV + rv * Cfg::RV_STAGE, Cfg::RV_CODES, sV + vs * Cfg::V_STAGE, ct,
+        convert_tile<KV, D, Cfg::V_RB, 32 * Cfg::NCONV>(sRV + rv * Cfg::RV_STAGE, Cfg::RV_CODES, sV + vs * Cfg::V_STAGE, ct,
                                        F - 64 * (p_lo + jj));
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(320, 1)
             // 16 f16 values are), q_hi in columns [COL_Q, COL_Q + D/4), q_lo
             // in the next D/4
             const int rk = j % NRK;
-            ok = mbar_wait_bounded(&k_full[rk], (j / NRK) & 1, a.status) && !*s_abort;
+            ok = mbar_wait_bounded(&rk_full[rk], (j / NRK) & 1, a.status) && !*s_abort;
             if (!ok) break;
             tc::fence_after();
             const uint64_t kd = tc::smem_desc(smem_u32(sRK + rk * Cfg::RK_STAGE), 16, 1024);
