@@ -39,15 +39,19 @@
 // INT8-G64 is the one profile whose dequantized values are not exact in f16:
 // an INT8 code (7 bits) times its binary16 group scale (11 bits) needs up to
 // 18 significant bits, and an exact form would need one fp32 accumulator per
-// 64-dim group of each key, four times the S columns of tensor memory.  Its
-// codes are dequantized as code * s_g computed exactly in fp32 and rounded
-// once to f16 (relative error <= 2^-11 per element), after a per-key power
-// of two 2^-e, e in [0, 7], that keeps the largest element of the key below
-// 2^15 (every binary16 scale is at most 65504, so every key fits f16); 2^e
-// goes into the key's fp32 factor (K) or its softmax weight (V), which stays
-// below 2^8 * 2^7 under the lazy 2^8 threshold.  Scores then differ from the
-// exact ones by at most 2^-11 of sum_d |q_d k_d| times the softmax scale, well
-// inside the attention tolerances.
+// 64-dim group of each key, four times the S columns of tensor memory.  A
+// per-key power of two 2^-e, e in [0, 7], keeps the largest element of the
+// key below 2^15 (every binary16 scale is at most 65504, so every key fits
+// f16); 2^e goes into the key's fp32 factor (K) or its softmax weight (V),
+// which stays below 2^8 * 2^7 under the lazy 2^8 threshold.  The codes are
+// then dequantized as code * s_g 2^-e with the scale a binary16 value and the
+// product rounded once to f16 (relative error <= 2^-11 per element).  The
+// scale s_g 2^-e is exact in binary16 whenever e = 0 (every key below 2^15,
+// all ordinary data) and otherwise unless the shift takes it below binary16's
+// normal range; there the element's error stays below 2^-25 * 127 of the
+// shifted scale, under 2^-32 of the key's largest element.  Scores then
+// differ from the exact ones by at most about 2^-11 of sum_d |q_d k_d| times
+// the softmax scale, well inside the attention tolerances.
 #include <cmath>
 
 #include "encode.cuh"
