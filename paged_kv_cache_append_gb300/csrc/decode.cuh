@@ -92,9 +92,11 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int KK, int KV, int D, int NQT>
 struct DecodeCfg {
-  // Head-dim split: at D = 256 the keys of a 16-key slab are shared by a pair
-  // of warps, each owning half of the dims (NH = 2); below, one warp per slab.
-  static constexpr int NH = D == 256 ? 2 : 1;
+  // Head-dim split: at D = 256 with more than 8 query rows, or over INT8
+  // pages (whose short contexts make the per-page latency count), the keys of
+  // a 16-key slab are shared by a pair of warps, each owning half of the dims
+  // (NH = 2); otherwise one warp per slab.
+  static constexpr int NH = (D == 256 && (NQT > 1 || KK == KIND_INT8)) ? 2 : 1;
   static constexpr int NW = 4 * NH;              // consumer warps
   static constexpr int NCONS = 32 * NW;          // consumer threads
   static constexpr int THREADS = NCONS + 32;     // + 1 producer warp
