@@ -127,12 +127,13 @@ struct DecodeCfg {
   static constexpr int OFF_Q = align_up(NSTAGE * STAGE > COMB ? NSTAGE * STAGE : COMB, 128);
   static constexpr int OFF_X = OFF_Q + align_up(R * Q_PITCH, 128);   // partial-S exchange [2][NW][32][NQT*4]
   static constexpr int OFF_RED = OFF_X + (NH == 2 ? 2 * NW * 32 * NQT * 4 * 4 : 0);
-  // per consumer warp: 16 keys x 64 dims of V as f16 (quantized V), the
-  // source of the ldmatrix.trans V^T fragments
+  // per consumer warp: its 16 keys x its dims of V as f16 (quantized V), in
+  // 64-dim blocks of 16 rows x 128 bytes, the source of the ldmatrix.trans
+  // V^T fragments
   // (head_dim <= 128: one warp per slab; at 256 the register bound of two
   // CTAs per SM keeps V^T in registers)
   static constexpr bool V_SMEM = KV != KIND_BF16 && NH == 1;
-  static constexpr int VW_BYTES = V_SMEM ? 16 * 128 : 0;
+  static constexpr int VW_BYTES = V_SMEM ? 16 * (D / NH) * 2 : 0;  // 16 keys x the warp's dims, f16
   static constexpr int OFF_VW = align_up(OFF_RED + 10 * R * 4, 128);
   static constexpr int OFF_BAR = OFF_VW + NW * VW_BYTES;  // m, l per pair; M, L per row
   static constexpr int MISC_INTS = 32;
@@ -744,12 +745,12 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         }
       }
     } else if constexpr (Cfg::V_SMEM) {
-      // The warp converts its 16 keys x DH dims of V to f16, 64 dims at a
-      // time, into its own scratch (key rows of 128 bytes, 128-byte swizzle),
+      // The warp converts its 16 keys x DH dims of V to f16 into its own
+      // scratch (64-dim blocks of 16 key rows x 128 bytes, 128-byte swizzle),
       // with the scales applied (NVFP4: an exact product; INT8 / FP8: the f16
       // product) and keys past the frontier zeroed; ldmatrix.trans then gives
       // the V^T fragments, as for BF16 pages.  Lane: key slab row kr = lane &
-      // 15, dims [32 dh, 32 dh + 32) of the chunk, dh = lane >> 4.
+      // 15, dims [32 dh, 32 dh + 32) of every 64-dim block, dh = lane >> 4.
       constexpr int RB = Cfg::V_RB;
       const uint8_t* vs_tile = st + Cfg::OFF_VS;
       const uint8_t* vtile = st + Cfg::OFF_V;
@@ -757,32 +758,44 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       const int kr = lane & 15, dh = lane >> 4;
       const int vkey = 16 * pair + kr;              // key of the page this lane converts
       const bool vlive = key0 + vkey < F;           // keys at or past the frontier are zero
+      __syncwarp();  // the previous page's fragments have been read
 #pragma unroll
       for (int q64 = 0; q64 < DH / 64; ++q64) {
-        __syncwarp();  // the previous chunk's fragments have been read
+        uint8_t* blk = vw + q64 * (16 * 128);
+        const int d0 = half * DH + 64 * q64 + 32 * dh;  // first of this lane's 32 dims
+        if constexpr (KV == KIND_NVFP4) {
+          const int colb = d0 / 2;  // 16 code bytes, two scale bytes
+          const uint4 w = *reinterpret_cast<const uint4*>(vtile + (colb / RB) * (64 * RB) + swz<RB>(vkey, colb % RB));
+          const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vs_tile + vkey * Cfg::VSB + d0 / 16));
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {  // 16 dims at a time
-          const int d0 = half * DH + 64 * q64 + 32 * dh + 16 * sub;  // first dim
-          uint32_t hv[8];                                            // 16 f16 of key vkey
-          if constexpr (KV == KIND_NVFP4) {
-            const int colb = d0 / 2;  // 8 code bytes, one scale byte
-            const uint2 w = *reinterpret_cast<const uint2*>(vtile + (colb / RB) * (64 * RB) + swz<RB>(vkey, colb % RB));
-            const uint32_t s1 = e4m3x2_to_f16x2(vs_tile[vkey * Cfg::VSB + d0 / 16]);
-            const uint32_t s2 = __byte_perm(s1, 0, 0x1010);
-            const uint32_t wv[2] = {w.x, w.y};
+          for (int sub = 0; sub < 2; ++sub) {  // 16 dims, one scale group
+            const uint32_t sq = __byte_perm(s2, 0, sub ? 0x3232 : 0x1010);
+            uint32_t hv[8];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-              hv[4 * q + 0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(wv[q]), s2);
-              hv[4 * q + 1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(wv[q]), s2);
-              hv[4 * q + 2] = hmul2_u32(e2m1x2_byte_to_f16x2<2>(wv[q]), s2);
-              hv[4 * q + 3] = hmul2_u32(e2m1x2_byte_to_f16x2<3>(wv[q]), s2);
+              hv[4 * q + 0] = hmul2_u32(e2m1x2_byte_to_f16x2<0>(wv[2 * sub + q]), sq);
+              hv[4 * q + 1] = hmul2_u32(e2m1x2_byte_to_f16x2<1>(wv[2 * sub + q]), sq);
+              hv[4 * q + 2] = hmul2_u32(e2m1x2_byte_to_f16x2<2>(wv[2 * sub + q]), sq);
+              hv[4 * q + 3] = hmul2_u32(e2m1x2_byte_to_f16x2<3>(wv[2 * sub + q]), sq);
             }
-          } else {  // INT8 / FP8: 16 code bytes
-            const uint4 w = *reinterpret_cast<const uint4*>(vtile + (d0 / RB) * (64 * RB) + swz<RB>(vkey, d0 % RB));
-            const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
-            const uint32_t s1 = KV == KIND_INT8 ? sp[vkey * (Cfg::VSB / 2) + d0 / 64] : sp[vkey];
-            const uint32_t s2 = s1 | (s1 << 16);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint4 v = vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
+                                    : make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(blk + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) = v;
+            }
+          }
+        } else {  // INT8 / FP8: 16 code bytes per 16 dims
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
+          const uint32_t s1 = KV == KIND_INT8 ? sp[vkey * (Cfg::VSB / 2) + d0 / 64] : sp[vkey];
+          const uint32_t s2 = s1 | (s1 << 16);
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            const int dd = d0 + 16 * sub;
+            const uint4 w = *reinterpret_cast<const uint4*>(vtile + (dd / RB) * (64 * RB) + swz<RB>(vkey, dd % RB));
             const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+            uint32_t hv[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               if constexpr (KV == KIND_INT8) {
@@ -793,21 +806,24 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
                 hv[2 * q + 1] = hmul2_u32(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[q] >> 16)), s2);
               }
             }
-          }
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint4 v = vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
-                                  : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(vw + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) = v;
+            for (int k = 0; k < 2; ++k) {
+              const uint4 v = vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
+                                    : make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(blk + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) = v;
+            }
           }
         }
-        __syncwarp();
+      }
+      __syncwarp();
 #pragma unroll
-        for (int mt4 = 0; mt4 < 4; ++mt4) {  // the chunk's four 16-dim m-tiles
+      for (int q64 = 0; q64 < DH / 64; ++q64) {
+#pragma unroll
+        for (int mt4 = 0; mt4 < 4; ++mt4) {  // the block's four 16-dim m-tiles
           const int key = (lane & 7) + ((lane >> 4) & 1) * 8;
           const int col = (16 * mt4 + 8 * ((lane >> 3) & 1)) * 2;
           uint32_t A[4];
-          ldsm_x4_t(smem_u32(vw) + swz<128>(key, col), A[0], A[1], A[2], A[3]);
+          ldsm_x4_t(smem_u32(vw + q64 * (16 * 128)) + swz<128>(key, col), A[0], A[1], A[2], A[3]);
 #pragma unroll
           for (int j = 0; j < NQT; ++j) mma16816<false>(o[4 * q64 + mt4][j], A, pb[0][j][0], pb[0][j][1]);
         }
