@@ -596,17 +596,30 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
       const float* ksc = sF + fs * 128;
       const float* vsc = ksc + 64;
       const int kmax = row_valid ? pos - 64 * (p_lo + j) : -1;
+      // Score factors: per key for FP8-row (row scale) and INT8-G64 (2^e)
+      // keys; NVFP4 keys carry their scales in the f16 values, so every key
+      // has the plain softmax scale.  The causal mask is applied only where
+      // the page reaches past a row's last key.
+      constexpr bool KEY_FAC = KK != KIND_NVFP4;
+      const bool nomask = __all_sync(0xffffffffu, kmax >= 63);
       float rmax = -INFINITY;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 k0 = *reinterpret_cast<const float4*>(ksc + 4 * c4);
-        const float4 k1 = *reinterpret_cast<const float4*>(ksc + 32 + 4 * c4);
-        const float ka[4] = {k0.x, k0.y, k0.z, k0.w}, kb[4] = {k1.x, k1.y, k1.z, k1.w};
+        float ka[4] = {a.scale_log2, a.scale_log2, a.scale_log2, a.scale_log2}, kb[4] = {ka[0], ka[1], ka[2], ka[3]};
+        if constexpr (KEY_FAC) {
+          const float4 k0 = *reinterpret_cast<const float4*>(ksc + 4 * c4);
+          const float4 k1 = *reinterpret_cast<const float4*>(ksc + 32 + 4 * c4);
+          ka[0] = k0.x, ka[1] = k0.y, ka[2] = k0.z, ka[3] = k0.w;
+          kb[0] = k1.x, kb[1] = k1.y, kb[2] = k1.z, kb[3] = k1.w;
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = 4 * c4 + u;
-          const float x = c <= kmax ? __uint_as_float(v0[c]) * ka[u] : -INFINITY;
-          const float y = 32 + c <= kmax ? __uint_as_float(v1[c]) * kb[u] : -INFINITY;
+          float x = __uint_as_float(v0[c]) * ka[u], y = __uint_as_float(v1[c]) * kb[u];
+          if (!nomask) {
+            x = c <= kmax ? x : -INFINITY;
+            y = 32 + c <= kmax ? y : -INFINITY;
+          }
           v0[c] = __float_as_uint(x);
           v1[c] = __float_as_uint(y);
           rmax = fmaxf(rmax, fmaxf(x, y));
@@ -622,13 +635,20 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
         resc = true;
       }
       const float mu = m_used == -INFINITY ? 0.f : m_used;
+      // Weight factors: FP8-row V (row scale) and INT8-G64 V (2^e); NVFP4 V
+      // carries its scales in the f16 values.
+      constexpr bool VAL_FAC = KV != KIND_NVFP4;
       uint32_t pk[32];
       float sum = 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 s0 = *reinterpret_cast<const float4*>(vsc + 4 * c4);
-        const float4 s1 = *reinterpret_cast<const float4*>(vsc + 32 + 4 * c4);
-        const float sa[4] = {s0.x, s0.y, s0.z, s0.w}, sbv[4] = {s1.x, s1.y, s1.z, s1.w};
+        float sa[4] = {1.f, 1.f, 1.f, 1.f}, sbv[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (VAL_FAC) {
+          const float4 s0 = *reinterpret_cast<const float4*>(vsc + 4 * c4);
+          const float4 s1 = *reinterpret_cast<const float4*>(vsc + 32 + 4 * c4);
+          sa[0] = s0.x, sa[1] = s0.y, sa[2] = s0.z, sa[3] = s0.w;
+          sbv[0] = s1.x, sbv[1] = s1.y, sbv[2] = s1.z, sbv[3] = s1.w;
+        }
         float p0[4], p1[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -636,10 +656,17 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
           p1[u] = ex2(fmaf(__uint_as_float(v1[4 * c4 + u]), rs, -mu));
           sum += p0[u] + p1[u];
         }
-        pk[2 * c4] = pack_f16x2(p0[0] * sa[0], p0[1] * sa[1]);
-        pk[2 * c4 + 1] = pack_f16x2(p0[2] * sa[2], p0[3] * sa[3]);
-        pk[16 + 2 * c4] = pack_f16x2(p1[0] * sbv[0], p1[1] * sbv[1]);
-        pk[16 + 2 * c4 + 1] = pack_f16x2(p1[2] * sbv[2], p1[3] * sbv[3]);
+        if constexpr (VAL_FAC) {
+          pk[2 * c4] = pack_f16x2(p0[0] * sa[0], p0[1] * sa[1]);
+          pk[2 * c4 + 1] = pack_f16x2(p0[2] * sa[2], p0[3] * sa[3]);
+          pk[16 + 2 * c4] = pack_f16x2(p1[0] * sbv[0], p1[1] * sbv[1]);
+          pk[16 + 2 * c4 + 1] = pack_f16x2(p1[2] * sbv[2], p1[3] * sbv[3]);
+        } else {
+          pk[2 * c4] = pack_f16x2(p0[0], p0[1]);
+          pk[2 * c4 + 1] = pack_f16x2(p0[2], p0[3]);
+          pk[16 + 2 * c4] = pack_f16x2(p1[0], p1[1]);
+          pk[16 + 2 * c4 + 1] = pack_f16x2(p1[2], p1[3]);
+        }
       }
       __syncwarp();
       if (lane == 0) q_arrive(&f_empty[fs]);  // this warp is done with the page's factors
