@@ -130,9 +130,9 @@ struct DecodeCfg {
   // per consumer warp: its 16 keys x its dims of V as f16 (quantized V), in
   // 64-dim blocks of 16 rows x 128 bytes, the source of the ldmatrix.trans
   // V^T fragments
-  // (head_dim <= 128: one warp per slab; at 256 the register bound of two
-  // CTAs per SM keeps V^T in registers)
-  static constexpr bool V_SMEM = KV != KIND_BF16 && NH == 1;
+  // (not for warp pairs launched two CTAs per SM: their register bound keeps
+  // V^T in registers)
+  static constexpr bool V_SMEM = KV != KIND_BF16 && (NH == 1 || (D / NH) * R / 32 > 32);
   static constexpr int VW_BYTES = V_SMEM ? 16 * (D / NH) * 2 : 0;  // 16 keys x the warp's dims, f16
   static constexpr int OFF_VW = align_up(OFF_RED + 10 * R * 4, 128);
   static constexpr int OFF_BAR = OFF_VW + NW * VW_BYTES;  // m, l per pair; M, L per row
