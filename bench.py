@@ -545,6 +545,8 @@ def extra_workloads(names, args, flush, stream, world, device, shared):
                             "frac": round(r["achieved"] / hbm_peak, 4),
                             "avg_launch_ms": round(r["kms"], 5), "timed_as": r["kms_how"]},
                "clocks": r["clocks"]}
+        if not b.Bp and w.B > 1 and not args.no_sweep:
+            ent["sweep_rows_per_s"] = sweep_rows(b, args, flush, stream, device)
         if b.Bp:
             ent["value_note"] = "decode-side GB/s of the whole step (prefill rows on a second stream)"
             ent["roofline"] = {"bound": "tensor", "kernel": "nk_paged_prefill_attention (tcgen05), one layer",
@@ -556,6 +558,23 @@ def extra_workloads(names, args, flush, stream, world, device, shared):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
     return out
+
+
+def sweep_rows(bench, args, flush, stream, device):
+    """Rows/s (and KV GB/s) of the step over the first c rows, c = 1..B, each
+    step replayed as its own graph (the rows share the filled pool)."""
+    import torch
+    w = bench.w
+    sweep = {}
+    for c in range(1, w.B + 1):
+        bc = Bench(w, device, B=c, share=bench, fused=bench.fused) if c != w.B else bench
+        g = _capture(torch, bc.step)
+        sm = _timed_graph(torch, g, max(5, args.steps // 4), flush, stream)[0]
+        sweep[str(c)] = {"rows_per_s": round(c * w.T / (sm * 1e-3), 1),
+                         "kv_gbs": round(bc.bytes_step() / (sm * 1e-3) / 1e9, 1),
+                         "ms_per_step": round(sm, 4)}
+        del g, bc
+    return sweep
 
 
 EXTRAS = {"k8v4_long": ["k8v4_verify", "int8_decode", "fp8_shared", "bf16_prefill"]}
@@ -630,14 +649,7 @@ def run_gpu(args, rank, world):
     # ---- rows/s at C = 1..8 ------------------------------------------------------
     sweep = {}
     if not args.no_sweep and w.B > 1:
-        for c in range(1, w.B + 1):
-            bc = Bench(w, device, B=c, share=bench, fused=bench.fused) if c != w.B else bench
-            g = _capture(torch, bc.step)
-            sm = _timed_graph(torch, g, max(5, args.steps // 4), flush, stream)[0]
-            sweep[str(c)] = {"rows_per_s": round(c * w.T / (sm * 1e-3), 1),
-                             "kv_gbs": round(bc.bytes_step() / (sm * 1e-3) / 1e9, 1),
-                             "ms_per_step": round(sm, 4)}
-            del g, bc
+        sweep = sweep_rows(bench, args, flush, stream, device)
 
     roof_kernel = "nk_paged_append_decode_attention" if bench.fused else "nk_paged_decode_attention"
     value = job_value(bench.bytes_step(), ms, world) / 1e9

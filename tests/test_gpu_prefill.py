@@ -216,3 +216,39 @@ def test_prefill_workspace_does_not_grow_with_the_context(profile):
         sizes.append(nk.nk_prefill_workspace_bytes(pool.handle, 2, 2048, 16))
         pool.close()
     assert sizes[0] == sizes[1], sizes
+
+
+@pytest.mark.parametrize("profile", ["fp8_row", "k8v4"])
+def test_fp8_key_prefill_with_an_outlier_query_channel(profile):
+    """FP8-row keys go to the tensor cores as raw E4M3 codes, with each query
+    row split into two E4M3 terms (hi + lo).  Elements below 2^-9 of the row's
+    largest one are kept to an absolute 2^-17 of it, so a query whose dim 5 is
+    30 times the others (small elements then fall below that edge) must still
+    match the oracle within the attention tolerances."""
+    w = prefill_workload(2, 8, 256, 1024, prefixes=[300, 61], chunks=[200, 150], Tc=256, seed=77,
+                         profile=profile)
+    sc = Scenario(w, layers=(0,), oracle=True)
+    dev = "cuda"
+    k, v = w.chunk_kv(0)
+    q = w.chunk_q(0).float()
+    q[..., 5] *= 30.0
+    q = q.to(torch.bfloat16)
+    rows = torch.from_numpy(w.prefill_rows).to(dev)
+    pre = torch.from_numpy(w.prefix_len).to(dev)
+    chk = torch.from_numpy(w.chunk_len).to(dev)
+    sc.gpu.append(0, sc.tables_d, rows, pre, k.to(dev), v.to(dev), counts=chk)
+    sc.orc.append(0, w.tables, w.prefill_rows, w.prefix_len, bf16_to_bits(k), bf16_to_bits(v), counts=w.chunk_len)
+    out, lse = sc.gpu.prefill(0, q.to(dev), sc.tables_d, rows, pre, chk, w.scale)
+    torch.cuda.synchronize()
+    out, lse = out.cpu(), lse.cpu()
+    qf = OF.bf16_bits_to_f64(bf16_to_bits(q))
+    for i, r in enumerate(w.prefill_rows):
+        P0, Cn = int(w.prefix_len[i]), int(w.chunk_len[i])
+        K, V = sc.orc.gather(0, w.tables[r], P0 + Cn)
+        toks = np.arange(0, Cn, 7)
+        ref_o = np.zeros((len(toks), w.Hq, w.D))
+        ref_l = np.zeros((len(toks), w.Hq))
+        for n_, t in enumerate(toks):
+            o1, l1 = OA.decode(qf[i, t:t + 1], K, V, P0 + t + 1, w.scale)
+            ref_o[n_], ref_l[n_] = o1[0], l1[0]
+        compare_attention(out[i, toks], lse[i, toks], ref_o, ref_l)
