@@ -543,15 +543,22 @@ def extra_workloads(names, args, flush, stream, world, device, shared):
                "roofline": {"bound": "hbm", "kernel": "decode call (decode + merge), one layer",
                             "achieved": round(r["achieved"], 1), "unit": "GB/s",
                             "frac": round(r["achieved"] / hbm_peak, 4),
+                            "traffic": traffic(name, "nk_paged_append_decode_attention", b.bytes_roofline_launch()),
+                            "algorithmic_bytes_per_launch": b.bytes_roofline_launch(),
                             "avg_launch_ms": round(r["kms"], 5), "timed_as": r["kms_how"]},
                "clocks": r["clocks"]}
+        if w.name == "tiny_bf16":  # latency-bound: one row, one layer, 200 tokens
+            ent["us_per_step"] = round(1e3 * r["ms"], 2)
         if not b.Bp and w.B > 1 and not args.no_sweep:
             ent["sweep_rows_per_s"] = sweep_rows(b, args, flush, stream, device)
         if b.Bp:
             ent["value_note"] = "decode-side GB/s of the whole step (prefill rows on a second stream)"
             ent["roofline"] = {"bound": "tensor", "kernel": "nk_paged_prefill_attention (tcgen05), one layer",
                                "achieved": round(r["tflops"], 1), "unit": "TFLOP/s",
-                               "frac": round(r["tflops"] / tf_peak, 4), "avg_launch_ms": round(r["pms"], 4),
+                               "frac": round(r["tflops"] / tf_peak, 4),
+                               "traffic": traffic(name, "nk_paged_prefill_attention", b.flops_prefill_layer()),
+                               "algorithmic_flops_per_launch": b.flops_prefill_layer(),
+                               "avg_launch_ms": round(r["pms"], 4),
                                "timed_as": "a graph of the prefill launches for all layers / layers"}
         out[name] = ent
         del r, b
@@ -577,7 +584,7 @@ def sweep_rows(bench, args, flush, stream, device):
     return sweep
 
 
-EXTRAS = {"k8v4_long": ["k8v4_verify", "int8_decode", "fp8_shared", "bf16_prefill"]}
+EXTRAS = {"k8v4_long": ["k8v4_verify", "int8_decode", "fp8_shared", "bf16_prefill", "tiny_bf16"]}
 
 
 def run_gpu(args, rank, world):
