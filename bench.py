@@ -316,8 +316,9 @@ class Bench:
             self.cout = [self.cout_buf[i * self.cq[0].numel() * 2:(i + 1) * self.cq[0].numel() * 2]
                          .view(torch.bfloat16).view(self.cq[0].shape) for i in range(w.num_layers)]
             self.side = torch.cuda.Stream(device=device)
-            # chunk append + prefill (+ the dequant pass of quantized pages) per layer
-            self.launches_per_step += (2 if w.profile == "bf16" else 3) * w.num_layers
+            # chunk append + prefill per layer (quantized pages are dequantized
+            # inside the prefill kernel)
+            self.launches_per_step += 2 * w.num_layers
 
     def _fill(self):
         """Context of every table row (device-side seeded values), written
