@@ -215,6 +215,13 @@ int nk_decode_workspace_bytes(const nk_pool* pool, int32_t B, int32_t T, int32_t
  * The split count per (row, KV head) is at most 32; at head_dim 64 and 128
  * the tensor-core kernel may take several splits per CTA.  Either way the
  * partials fit the workspace that nk_decode_workspace_bytes reports.
+ * Keys enter the scores exactly (row and group scales multiply fp32 partial
+ * scores).  In the warp-level kernel INT8-G64 and FP8-row values are f16
+ * products code * scale * 2^K (relative error <= 2^-11 above f16's subnormal
+ * range), K <= 0 lowered where needed so that no product overflows; in the
+ * tensor-core kernel FP8-row value scales multiply the f16 softmax weights,
+ * lifted by 2^K so that they stay finite and normal.  Either way 2^K is
+ * removed before the output, so V of any magnitude is handled.
  * Errors: NK_ERR_INVALID_ARG, NK_ERR_SHAPE (Hq % H, B > C, T < 1),
  * NK_ERR_UNSUPPORTED (R > 32, or R > 16 at head_dim 256 over BF16 or
  * INT8-G64 pools), NK_ERR_ALIGN, NK_ERR_WORKSPACE, NK_ERR_CUDA. */
@@ -317,9 +324,14 @@ int nk_prefill_workspace_bytes(const nk_pool* pool, int32_t B, int32_t Tc, int32
 /* Chunked prefill / replay attention through the block tables (every
  * profile; quantized pages are dequantized inside the tensor-core kernel,
  * page tile by page tile in shared memory, with no copy of the context
- * elsewhere.  The tiles hold FP8-row, NVFP4-G16 and K8V4 values exactly;
- * INT8-G64 values, code times group scale, are rounded once to f16, relative
- * error <= 2^-11).
+ * elsewhere.  The tiles hold FP8-row, NVFP4-G16 and K8V4 keys and values
+ * and INT8-G64 keys exactly (an INT8-G64 key tile as two f16 tiles whose sum
+ * is code times group scale); INT8-G64 values are rounded once to f16,
+ * relative error <= 2^-11.  Softmax weights are f16 over quantized pools,
+ * with FP8-row value scales applied under a power-of-two lift that keeps
+ * them in f16's normal range for V of any magnitude, and bf16 over BF16
+ * pools: relative error <= 2^-8 per weight, so there the output is within
+ * 2^-8 of the attention over |V| of the exact one, beyond fp32 rounding).
  * Query i < chunk_len[b] of row b sits at logical position prefix_len[b] + i
  * and attends keys j <= prefix_len[b] + i; the chunk's own K/V must already
  * be appended.  Prefill work is proportional to prefix*S + S(S+1)/2 query-key

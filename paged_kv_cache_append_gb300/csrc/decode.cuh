@@ -496,6 +496,13 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   // ---- running state -----------------------------------------------------------
   float m_run[NQT][2], l_part[NQT][2];
   float o[MTW][NQT][4];
+  // INT8-G64 / FP8-row V: the values are f16 products code * (s 2^k_run), with
+  // k_run <= 0 the lift of the largest value scale this warp has read
+  // (v_lift): 0 for every V below 2^7 * 127 (INT8) or 2^7 * 448 (FP8), less
+  // above, so that no product overflows f16 whatever the magnitude of V.  O
+  // carries 2^k_run and is rescaled when it drops; the combine removes it.
+  constexpr bool V_LIFT = KV == KIND_INT8 || KV == KIND_FP8;
+  int k_run = 0;
 #pragma unroll
   for (int j = 0; j < NQT; ++j) {
     m_run[j][0] = m_run[j][1] = -INFINITY;
@@ -530,6 +537,27 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       break;
     }
     const int key0 = (p0 + i) * 64;
+
+    // V lift: the largest scale of this warp's 16 keys below the frontier
+    // (lane: key 16 pair + lane % 16; INT8 groups of the warp's dims split by
+    // lane / 16), across the warp
+    int knew = k_run;
+    if constexpr (V_LIFT) {
+      const uint16_t* vsp = reinterpret_cast<const uint16_t*>(st + Cfg::OFF_VS);
+      const int vk = 16 * pair + (lane & 15);
+      float smax = 0.f;
+      if (key0 + vk < F) {
+        if constexpr (KV == KIND_INT8) {
+          constexpr int GW = DH >= 64 ? DH / 64 : 1;
+#pragma unroll
+          for (int gi = lane >> 4; gi < GW; gi += 2)
+            smax = fmaxf(smax, __half2float(__ushort_as_half(vsp[vk * (Cfg::VSB / 2) + (half * DH) / 64 + gi])));
+        } else {
+          smax = __half2float(__ushort_as_half(vsp[vk]));
+        }
+      }
+      knew = v_lift(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)), k_run);
+    }
 
     // ---------------- QK: partial S^T over this warp's head dims ------------------
     float S[NQT][4];
@@ -687,17 +715,20 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         l_part[j][u] = l_part[j][u] * alpha[j][u] + S[j][u] + S[j][2 + u];
       }
     }
-    if (__any_sync(0xffffffffu, rescale)) {
+    if (__any_sync(0xffffffffu, rescale) || knew != k_run) {
+      const float kf = pow2i(knew - k_run);
 #pragma unroll
       for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
         for (int j = 0; j < NQT; ++j) {
-          o[mt][j][0] *= alpha[j][0];
-          o[mt][j][1] *= alpha[j][1];
-          o[mt][j][2] *= alpha[j][0];
-          o[mt][j][3] *= alpha[j][1];
+          o[mt][j][0] *= alpha[j][0] * kf;
+          o[mt][j][1] *= alpha[j][1] * kf;
+          o[mt][j][2] *= alpha[j][0] * kf;
+          o[mt][j][3] *= alpha[j][1] * kf;
         }
     }
+    k_run = knew;
+    const uint32_t lift2 = static_cast<uint32_t>(k_run + 15) * 0x04000400u;  // f16x2 (2^k_run, 2^k_run)
     // P^T as the B operand of PV, straight from registers: (key r, rows 2c,2c+1)
     // transposed by movmatrix gives (row r, keys 2c, 2c+1).
     uint32_t pb[Cfg::MMA_BF16 ? 2 : 1][NQT][2];
@@ -789,7 +820,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         } else {  // INT8 / FP8: 16 code bytes per 16 dims
           const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
           const uint32_t s1 = KV == KIND_INT8 ? sp[vkey * (Cfg::VSB / 2) + d0 / 64] : sp[vkey];
-          const uint32_t s2 = s1 | (s1 << 16);
+          const uint32_t s2 = hmul2_u32(s1 | (s1 << 16), lift2);
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {
             const int dd = d0 + 16 * sub;
@@ -873,6 +904,8 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
             slo = sp[keys[0]] | (uint32_t(sp[keys[1]]) << 16);
             shi = sp[keys[2]] | (uint32_t(sp[keys[3]]) << 16);
           }
+          slo = hmul2_u32(slo, lift2);
+          shi = hmul2_u32(shi, lift2);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if constexpr (KV == KIND_INT8) {
@@ -941,12 +974,13 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   float* comb = reinterpret_cast<float*>(smem);
   {
     float fac[NQT][2];
+    const float unlift = pow2i(-k_run);  // O carries 2^k_run (1 but for quantized V near the f16 limit)
 #pragma unroll
     for (int j = 0; j < NQT; ++j)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float M = row_M[8 * j + 2 * c + u];
-        fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M);
+        fac[j][u] = M == -INFINITY ? 0.f : ex2(m_run[j][u] - M) * unlift;
       }
     float* mine = comb + pair * R * D;
 #pragma unroll

@@ -179,6 +179,30 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^k as a float, for -126 <= k <= 127 (exact).
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
+
+// ------------------------------------------------------------ FP8-row V lift
+// Kernels that apply FP8-row value scales to the softmax weights store
+// p * s_key as f16 operands of P V, with p <= 2^8 (the lazy rescale
+// threshold).  Raw, p * s would leave f16's normal range for small V (s is
+// amax / 448) and overflow for V near the binary16 limit.  The weights are
+// therefore lifted by a power of two 2^K chosen from the largest scale s_max
+// seen so far, s_max 2^K in [2^6, 2^7): every lifted weight stays below 2^15
+// and the large ones far above the subnormal range, whatever the magnitude
+// of V.  K only decreases along a row's keys (the accumulators are rescaled
+// when it does) and starts at kVLiftInit, the value for the smallest positive
+// binary16 scale, 2^-24.
+constexpr int kVLiftTop = 6, kVLiftInit = kVLiftTop + 24, kVLiftMin = kVLiftTop - 15;
+
+// K after a tile whose largest value scale has the bits smax_bits (a
+// non-negative float; 0 when every scale of the tile is zero: K stays).  K is
+// at least kVLiftMin, the value for the largest binary16 scale, 65504.
+__device__ __forceinline__ int v_lift(uint32_t smax_bits, int k_run) {
+  if (smax_bits == 0u) return k_run;
+  return min(k_run, max(kVLiftTop + 127 - static_cast<int>(smax_bits >> 23), kVLiftMin));
+}
+
 // Two E4M3FN codes (low byte = element 0) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
@@ -240,6 +264,13 @@ __device__ __forceinline__ uint32_t s8pair_to_f16x2(uint32_t w_pair_in_bytes_0_2
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// a * b + c on f16x2, rounded once
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                      *reinterpret_cast<const __half2*>(&c));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 

@@ -34,24 +34,28 @@
 //   * q is scaled per query row by a power of two, 2^e with max|q| 2^e in
 //     [2^14, 2^15), which makes bf16 -> f16 exact for every element above
 //     max|q| 2^-31; the scores divide 2^e back out in fp32.
-// With FP8-row V the weights p * s_key must stay finite in f16, so the running
-// maximum is exact (p <= 1); NVFP4 V keeps the lazy 2^8 rescale threshold.
-// INT8-G64 is the one profile whose dequantized values are not exact in f16:
-// an INT8 code (7 bits) times its binary16 group scale (11 bits) needs up to
-// 18 significant bits, and an exact form would need one fp32 accumulator per
-// 64-dim group of each key, four times the S columns of tensor memory.  A
-// per-key power of two 2^-e, e in [0, 7], keeps the largest element of the
-// key below 2^15 (every binary16 scale is at most 65504, so every key fits
-// f16); 2^e goes into the key's fp32 factor (K) or its softmax weight (V),
-// which stays below 2^8 * 2^7 under the lazy 2^8 threshold.  The codes are
-// then dequantized as code * s_g 2^-e with the scale a binary16 value and the
-// product rounded once to f16 (relative error <= 2^-11 per element).  The
-// scale s_g 2^-e is exact in binary16 whenever e = 0 (every key below 2^15,
-// all ordinary data) and otherwise unless the shift takes it below binary16's
-// normal range; there the element's error stays below 2^-25 * 127 of the
-// shifted scale, under 2^-32 of the key's largest element.  Scores then
-// differ from the exact ones by at most about 2^-11 of sum_d |q_d k_d| times
-// the softmax scale, well inside the attention tolerances.
+// Every profile rescales lazily (a row's maximum moves only when a score
+// passes it by more than 2^8, so p <= 2^8).  FP8-row V weights p * s_key are
+// lifted by a power of two 2^K, s_max 2^K in [2^6, 2^7) for the largest V
+// scale seen so far (v_lift), so that they stay finite and far from f16's
+// subnormal range for V of any magnitude; 2^K is carried by l and O alike and
+// leaves with the row's maximum (m - K) in the epilogue.
+// INT8-G64 is the one profile whose dequantized values are not f16 values: an
+// INT8 code (7 bits) times its binary16 group scale (11 bits) needs up to 18
+// significant bits.  A per-key power of two 2^-e, e in [0, 7], keeps the
+// largest element of the key below 2^15 (every binary16 scale is at most
+// 65504, so every key fits f16); 2^e goes into the key's fp32 factor (K) or
+// its softmax weight (V), which stays below 2^8 * 2^7 under the lazy 2^8
+// threshold.  With s' = s_g 2^-e as a binary16 value (exact whenever e = 0,
+// i.e. every key below 2^15, and otherwise unless the shift takes it below
+// binary16's normal range, where the element's error stays under 2^-32 of the
+// key's largest element):
+//   * keys are exact: each K tile is held as two f16 tiles k1 = f16(c s') and
+//     k2 = c s' - k1 (an f16 value, see convert_tile), and S accumulates
+//     Q k1^T + Q k2^T, so the scores are those of the dequantized keys up to
+//     the fp32 accumulation;
+//   * values are rounded once, c s' to f16 (relative error <= 2^-11 per
+//     element, as the f16 softmax weights themselves).
 #include <cmath>
 
 #include "encode.cuh"
@@ -73,7 +77,6 @@ struct QArgs {
   float* lse;
   int* status;
   float scale_log2;  // softmax_scale * log2(e)
-  float thr;         // rescale threshold in log2 units
   int B, Tc, Hq, H, G, L, M, C;
   PrefillSplit sp;
   int head_major;  // plane order
@@ -96,6 +99,10 @@ __device__ __forceinline__ int int8_row_shift(const uint8_t* scale_row) {
 // 2^-e for e in [0, 7] (a normal fp32).
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
+// Rescale threshold of the online softmax, in log2 units: the running maximum
+// moves only when a score passes it by more than this, so p <= 2^8.
+constexpr float kLazyThr = 8.f;
+
 template <int KK, int KV, int D>
 struct QCfg {
   // converter warps (6 .. 5 + NCONV): 8 where K and V are both converted, 4
@@ -106,7 +113,9 @@ struct QCfg {
   static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
   static constexpr int K_RB = KCB < 128 ? KCB : 128, V_RB = VCB < 128 ? VCB : 128;
   static constexpr int F16 = 64 * D * 2;                           // one f16 page tile
-  static constexpr int K_STAGE = F16;
+  // INT8-G64 keys are held as two f16 tiles whose sum is exact (K_SPLIT)
+  static constexpr bool K_SPLIT = KK == KIND_INT8;
+  static constexpr int K_STAGE = K_SPLIT ? 2 * F16 : F16;
   static constexpr int V_STAGE = F16;
   static constexpr int NF = 4;                                     // factor ring (512 B per page)
   static constexpr int RK_CODES = (64 * KCB + 1023) / 1024 * 1024;  // raw K code tile (1024-aligned)
@@ -117,8 +126,9 @@ struct QCfg {
   // f16 tiles) go to the tensor cores as raw E4M3 codes (kind::f8f6f4), with
   // q split exactly into two E4M3 terms: no K conversion, no f16 K tile.
   static constexpr bool K8MMA = (KK == KIND_FP8) && D >= 128;
-  static constexpr int NK = K8MMA ? 0 : D == 256 ? 2 : D == 128 ? 4 : 6;  // f16 K ring
-  static constexpr int NV = K8MMA ? (D == 256 ? 3 : 4) : NK;              // f16 V ring
+  static constexpr int NK = K8MMA ? 0 : K_SPLIT ? (D == 256 ? 1 : D == 128 ? 3 : 6)
+                                              : D == 256 ? 2 : D == 128 ? 4 : 6;  // f16 K ring
+  static constexpr int NV = K8MMA ? (D == 256 ? 3 : 4) : K_SPLIT ? (D == 256 ? 2 : D == 128 ? 3 : 6) : NK;  // f16 V ring
   static constexpr int NRK = K8MMA ? (D == 256 ? 3 : 6) : D == 256 ? (RK_STAGE <= 10240 ? 3 : 2) : 4;  // raw rings
   static constexpr int NRV = D == 256 ? (RV_STAGE <= 10240 || K8MMA ? 3 : 2) : 4;
   static constexpr int NKF = K8MMA ? 0 : NK;  // f16 K ready barriers (the raw FP8 keys need none)
@@ -216,11 +226,18 @@ __device__ __forceinline__ float key_factor(const uint8_t* scales, int r) {
 // ahead, which keeps the 8-byte NVFP4 loads (16 threads per access) apart.
 // NCT, the number of converter threads, is a multiple of 64; keys at or past
 // `kvalid` become zeros.
-template <int KIND, int D, int RB, int NCT>
+//
+// SPLIT (INT8-G64 only): the tile is written twice, as k1 = f16(c s') and, at
+// f16 + 64 D 2, as k2 = f16(c s' - k1), with s' = s_g 2^-e the binary16
+// scale.  c s' is a multiple of 2^-24 with at most 7 + 11 significant bits, so
+// the remainder c s' - k1 (at most 7 bits, the same multiple) is an f16 value
+// and k1 + k2 = c s' exactly: one f16 FMA per pair gives it.
+template <int KIND, int D, int RB, int NCT, bool SPLIT = false>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, uint8_t* f16, int ct, int kvalid) {
   constexpr int GPR = D / 16;            // 16-dim groups per key
   constexpr int UPT = (64 * GPR) / NCT;  // units per thread
   static_assert(UPT * NCT == 64 * GPR && UPT >= 1, "converter units");
+  static_assert(!SPLIT || KIND == KIND_INT8, "split tiles are for INT8-G64 keys");
   constexpr int SB = scale_row_bytes<KIND>(D);
   const uint8_t* scales = raw + raw_codes;
   int rr[UPT], gg[UPT];
@@ -231,6 +248,40 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
   }
   float shift = 1.f;
   if constexpr (KIND == KIND_INT8) shift = pow2_neg(int8_row_shift<D>(scales + rr[0] * SB));
+  if constexpr (SPLIT) {
+    // raw codes and scaled scales of every unit first, then convert and store
+    uint4 w[UPT];
+    uint32_t s2[UPT];
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      w[k] = *reinterpret_cast<const uint4*>(raw + raw_off<RB>(rr[k], 16 * gg[k]));
+      const __half s16 = __float2half_rn(
+          __half2float(*reinterpret_cast<const __half*>(scales + rr[k] * SB + 2 * ((16 * gg[k]) / 64))) * shift);
+      s2[k] = pack_h2(s16, s16);
+    }
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      const uint32_t wv[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+      uint32_t k1[8], k2[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t c0 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x1100));
+        const uint32_t c1 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x3322));
+        k1[2 * q] = hmul2_u32(c0, s2[k]);
+        k1[2 * q + 1] = hmul2_u32(c1, s2[k]);
+        k2[2 * q] = hfma2_u32(c0, s2[k], k1[2 * q] ^ 0x80008000u);
+        k2[2 * q + 1] = hfma2_u32(c1, s2[k], k1[2 * q + 1] ^ 0x80008000u);
+      }
+      const bool z = rr[k] >= kvalid;
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t o0 = f16_off(rr[k], 16 * gg[k]), o1 = f16_off(rr[k], 16 * gg[k] + 8);
+      *reinterpret_cast<uint4*>(f16 + o0) = z ? zero : make_uint4(k1[0], k1[1], k1[2], k1[3]);
+      *reinterpret_cast<uint4*>(f16 + o1) = z ? zero : make_uint4(k1[4], k1[5], k1[6], k1[7]);
+      *reinterpret_cast<uint4*>(f16 + 128 * D + o0) = z ? zero : make_uint4(k2[0], k2[1], k2[2], k2[3]);
+      *reinterpret_cast<uint4*>(f16 + 128 * D + o1) = z ? zero : make_uint4(k2[4], k2[5], k2[6], k2[7]);
+    }
+    return;
+  }
   uint4 lo[UPT], hi[UPT];
   // every raw load of the thread before any store (the stores could alias)
 #pragma unroll
@@ -402,7 +453,8 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
           const int ks = i % NK;
           if (i >= NK) ok = mbar_wait_bounded(&k_empty[ks], ((i / NK) - 1) & 1, a.status) && !*s_abort;
           if (!ok) break;
-          convert_tile<KK, D, Cfg::K_RB, 32 * Cfg::NCONV>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct, kvalid);
+          convert_tile<KK, D, Cfg::K_RB, 32 * Cfg::NCONV, Cfg::K_SPLIT>(raw, Cfg::RK_CODES, sK + ks * Cfg::K_STAGE, ct,
+                                                                       kvalid);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
@@ -473,11 +525,16 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
             ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status) && !*s_abort;
             if (!ok) break;
             tc::fence_after();
-            const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE), 16, 1024);
+            // INT8-G64: the two f16 tiles of the split keys accumulate into S
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
-                         kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S, kk > 0);
+            for (int part = 0; part < (Cfg::K_SPLIT ? 2 : 1); ++part) {
+              const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE + part * Cfg::F16), 16, 1024);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
+                           kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S,
+                           part > 0 || kk > 0);
+            }
             tc::commit(&s_full[sb]);
             tc::commit(&k_empty[ks]);
           }
@@ -582,6 +639,7 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
       if (lane == 0) q_arrive(q_ready);
     }
     float m_used = -INFINITY, l = 0.f;
+    int k_run = KV == KIND_FP8 ? kVLiftInit : 0;  // FP8-row V: the weights, l and O carry 2^k_run (v_lift)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1, fs = j % NF;
@@ -626,18 +684,28 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
         }
       }
       rmax = rmax == -INFINITY ? -INFINITY : rmax * rs;
-      float factor = 1.f;
-      const float mnew = fmaxf(m_used, rmax);
-      bool resc = false;
-      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + a.thr)) {
-        factor = m_used == -INFINITY ? 0.f : ex2(m_used - mnew);
-        m_used = mnew;
-        resc = true;
-      }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
       // Weight factors: FP8-row V (row scale) and INT8-G64 V (2^e); NVFP4 V
       // carries its scales in the f16 values.
       constexpr bool VAL_FAC = KV != KIND_NVFP4;
+      // FP8-row V: the lift of the largest row scale so far (every lane
+      // reads two of the page's 64 scales; the maximum crosses the warp)
+      int knew = k_run;
+      if constexpr (KV == KIND_FP8) {
+        const float2 s2 = *reinterpret_cast<const float2*>(vsc + 2 * lane);
+        knew = v_lift(__reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(s2.x, s2.y))), k_run);
+      }
+      // p = 2^(z - m + K): a rescale when the maximum passes the lazy
+      // threshold or the lift drops
+      float factor = 1.f;
+      const float mnew = fmaxf(m_used, rmax);
+      bool resc = false;
+      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + kLazyThr || knew != k_run)) {
+        factor = m_used == -INFINITY ? 0.f : ex2((m_used - mnew) + static_cast<float>(knew - k_run));
+        m_used = mnew;
+        resc = true;
+      }
+      k_run = knew;
+      const float mu = m_used == -INFINITY ? 0.f : m_used - static_cast<float>(k_run);
       uint32_t pk[32];
       float sum = 0.f;
 #pragma unroll
@@ -699,7 +767,8 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
     if (ok) {
       const int64_t orow = (static_cast<int64_t>(b) * a.Tc + token) * a.Hq + h * G + g;
       const int64_t tile = (static_cast<int64_t>(b) * a.H + h) * a.sp.tiles + qt;
-      prefill_store<D>(tmem + lane_base + Cfg::COL_O, n > 0, row_valid, m_used, l, a.out + orow * D,
+      const float m_eff = m_used == -INFINITY ? -INFINITY : m_used - static_cast<float>(k_run);
+      prefill_store<D>(tmem + lane_base + Cfg::COL_O, n > 0, row_valid, m_eff, l, a.out + orow * D,
                        a.lse ? a.lse + orow : nullptr, a.sp, tile, split, m, s_last);
     }
   }
@@ -757,7 +826,6 @@ int qprefill_launch(const nk_pool* p, int layer, const void* q, const int32_t* t
   a.lse = lse;
   a.status = p->status;
   a.scale_log2 = scale_log2;
-  a.thr = p->desc.profile == NK_FP8_E4M3_ROW ? 0.f : 8.f;  // FP8-row V carries its scales in P
   a.B = B;
   a.Tc = Tc;
   a.Hq = Hq;

@@ -24,8 +24,9 @@
 //   O += P V    tcgen05.mma M 128 x N D x K TK; P (f16) over its S buffer.
 // Operands are exact: E4M3 and E2M1 codes are f16 values, an E2M1 code times
 // its E4M3 scale is an exact f16 product, FP8-row key scales multiply the fp32
-// scores and FP8-row value scales the softmax weights (with an exact running
-// maximum, so p * s stays finite in f16).
+// scores and FP8-row value scales the softmax weights.  Rows rescale lazily
+// (p <= 2^8); FP8-row weights p * s are lifted by 2^K (v_lift), so that they
+// stay finite and clear of f16's subnormal range for V of any magnitude.
 //
 // Layout of the query rows.  Query row r sits in TMEM lane 32 (r / 8) + r % 8,
 // so that each of the four lane quadrants (and each warp scheduler) holds 8
@@ -81,7 +82,7 @@ struct VCfg {
   static_assert(COL_O + D <= 512 && COL_Q + D / 2 <= 512 && TK * NSB <= 256, "TMEM columns");
   static constexpr uint32_t ID_S = tc::idesc_f16(128, TK, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, D, false, true);
-  static constexpr float THR = KV == KIND_FP8 ? 0.f : 8.f;  // exact maximum when P carries V scales
+  static constexpr float THR = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
   static_assert(RPT * (D / 8) == 32 * NDW && PASSES * RPT == 64 && RPT % 8 == 0, "unit map");
 };
@@ -545,6 +546,7 @@ __global__ void __launch_bounds__(448, 1)
     }
     const float rs = __shfl_sync(0xffffffffu, rs_q, rl);
     float m_used = -INFINITY, l = 0.f;
+    int k_run = KV == KIND_FP8 ? kVLiftInit : 0;  // FP8-row V: the weights, l and O carry 2^k_run (v_lift)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int sb = j % NSB, ss = j % NS;
@@ -599,15 +601,28 @@ __global__ void __launch_bounds__(448, 1)
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
       const float rmax = pm == -INFINITY ? -INFINITY : pm * rs;
+      // FP8-row V: the lift of the largest value scale so far (the tile's
+      // scales are read across the warp, zero past the frontier)
+      int knew = k_run;
+      if constexpr (KV == KIND_FP8) {
+        const float* vs_all = sSc + ss * 2 * TK + TK;
+        float smax = 0.f;
+#pragma unroll
+        for (int i = 0; i < TK / 32; ++i) smax = fmaxf(smax, vs_all[32 * i + lane]);
+        knew = v_lift(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)), k_run);
+      }
+      // p = 2^(z - m + K): a rescale when the maximum passes the lazy
+      // threshold or the lift drops
       float factor = 1.f;
       const float mnew = fmaxf(m_used, rmax);
       bool resc = false;
-      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + Cfg::THR)) {
-        factor = m_used == -INFINITY ? 0.f : ex2(m_used - mnew);
+      if (mnew != -INFINITY && (m_used == -INFINITY || mnew > m_used + Cfg::THR || knew != k_run)) {
+        factor = m_used == -INFINITY ? 0.f : ex2((m_used - mnew) + static_cast<float>(knew - k_run));
         m_used = mnew;
         resc = true;
       }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      k_run = knew;
+      const float mu = m_used == -INFINITY ? 0.f : m_used - static_cast<float>(k_run);
       uint32_t pk[NREP * 2];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -672,7 +687,8 @@ __global__ void __launch_bounds__(448, 1)
     float lr = l + __shfl_xor_sync(0xffffffffu, l, 1);
     lr += __shfl_xor_sync(0xffffffffu, lr, 2);
     const float lt = __shfl_sync(0xffffffffu, lr, 4 * (lane & 7));
-    const float mt_row = __shfl_sync(0xffffffffu, m_used, 4 * (lane & 7));
+    const float m_eff = m_used == -INFINITY ? -INFINITY : m_used - static_cast<float>(k_run);
+    const float mt_row = __shfl_sync(0xffffffffu, m_eff, 4 * (lane & 7));
     const int orow = 8 * warp + lane;
     const bool out_real = lane < 8 && orow < R_real;
     const int ot = orow / a.G, og = orow % a.G;
@@ -785,7 +801,7 @@ struct VTCfg {
   static constexpr uint32_t COL_K = 0, COL_S = NK * D / 2, COL_O = COL_S + NSB * 32;
   static constexpr uint32_t ID_S = tc::idesc_f16(128, 32, false, false);
   static constexpr uint32_t ID_O = tc::idesc_f16(128, 32, true, false);
-  static constexpr float THR = KV == KIND_FP8 ? 0.f : 8.f;  // exact maximum when P carries V scales
+  static constexpr float THR = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8
   static_assert(D == 64 || D == 128, "transposed form");
   static_assert(NR >= 2 * PPT && NR * RAW >= CHUNK, "raw stages");
   static_assert(COL_O + 32 <= 512, "TMEM columns");
@@ -1322,6 +1338,7 @@ __global__ void __launch_bounds__(448, 1)
       for (int r = 0; r < 32; ++r) lacc[r] = 0.f;
       float m_self = -INFINITY;        // the running maximum of row `lane`
       uint32_t inf_rows = 0xffffffffu;  // rows whose running maximum is still -inf
+      int k_run = KV == KIND_FP8 ? kVLiftInit : 0;  // FP8-row V: the weights and O^T carry 2^k_run (v_lift)
       for (int j = 0; j < nt; ++j) {
         const int jg = J + j, sb = jg % NSB, ss = jg % NS;
         ok = mbar_wait_bounded(&s_full[sb], (jg / NSB) & 1, a.status) && !*s_abort;
@@ -1424,7 +1441,17 @@ __global__ void __launch_bounds__(448, 1)
         // P = 2^t, stored as f16 into column kq of the K-major P^T tile
         const uint32_t pb = p_col + sb * Cfg::PB;
         float vsc = 1.f;
-        if constexpr (KV == KIND_FP8) vsc = sSc[ss * 2 * TK + TK + kq];
+        int knew = k_run;
+        if constexpr (KV == KIND_FP8) {
+          // the lift of the largest value scale so far (the tile's scales
+          // are read across the warp, zero past the frontier); l stays unlifted
+          const float* vs_all = sSc + ss * 2 * TK + TK;
+          float smax = 0.f;
+#pragma unroll
+          for (int u = 0; u < TK / 32; ++u) smax = fmaxf(smax, vs_all[32 * u + lane]);
+          knew = v_lift(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)), k_run);
+          vsc = vs_all[kq] * pow2i(knew);
+        }
 #pragma unroll
         for (int r = 0; r < 32; r += 2) {
           const float p0v = ex2(t[r]), p1v = ex2(t[r + 1]);
@@ -1434,10 +1461,12 @@ __global__ void __launch_bounds__(448, 1)
           st_shared_u16(pb + swz<128>(r, p_byte), static_cast<uint16_t>(w & 0xFFFFu));
           st_shared_u16(pb + swz<128>(r + 1, p_byte), static_cast<uint16_t>(w >> 16));
         }
-        if (moved && j >= 1) {
-          // O^T is rescaled only when a row's maximum moved: O^T += V^T P^T(J - 1)
-          // must have landed first (the one before it has, as S^T(J) has completed);
-          // O^T += V^T P^T(J) waits for this warp's P^T
+        if ((moved || knew != k_run) && j >= 1) {
+          // O^T is rescaled only when a row's maximum moved or the lift
+          // dropped: O^T += V^T P^T(J - 1) must have landed first (the one
+          // before it has, as S^T(J) has completed); O^T += V^T P^T(J) waits
+          // for this warp's P^T
+          const float kf = pow2i(knew - k_run);
           const int jp = jg - 1;
           if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[jp % NSB], (jp / NSB) & 1, a.status) && !*s_abort)) {
             ok = false;
@@ -1452,11 +1481,12 @@ __global__ void __launch_bounds__(448, 1)
             tc::wait_ld();
 #pragma unroll
             for (int r = 0; r < 16; ++r)
-              ov[r] = __float_as_uint(__uint_as_float(ov[r]) * __shfl_sync(0xffffffffu, fac, c0 + r));
+              ov[r] = __float_as_uint(__uint_as_float(ov[r]) * (__shfl_sync(0xffffffffu, fac, c0 + r) * kf));
             tc::st16(tmem + lq + Cfg::COL_O + c0, ov);
           }
           tc::wait_st();
         }
+        k_run = knew;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc::fence_before();
         __syncwarp();
@@ -1476,7 +1506,8 @@ __global__ void __launch_bounds__(448, 1)
         const int b = g0.b;
         const bool final_out = g0.ns == 1;
         const int64_t part = (static_cast<int64_t>(b) * a.H + h) * a.target + g0.k;
-        const float inv_self = lt > 0.f ? 1.f / lt : 0.f;
+        const float unlift = KV == KIND_FP8 ? pow2i(-k_run) : 1.f;  // O^T carries 2^k_run
+        const float inv_self = lt > 0.f ? unlift / lt : 0.f;
         const int dim = 32 * warp + lane;  // O^T lane: the dimension this thread writes
         uint32_t ov[32];
         if (n > 0) {
@@ -1500,7 +1531,7 @@ __global__ void __launch_bounds__(448, 1)
                 a.out[((static_cast<int64_t>(b) * a.T + ot) * a.Hq + h * a.G + og) * D + dim] =
                     __float2bfloat16_rn(__uint_as_float(ov[r]) * inv);
               } else {
-                a.ws_acc[(part * R + r) * D + dim] = __uint_as_float(ov[r]);
+                a.ws_acc[(part * R + r) * D + dim] = __uint_as_float(ov[r]) * unlift;
               }
             }
           }

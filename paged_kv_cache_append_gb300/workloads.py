@@ -71,6 +71,9 @@ class Workload:
     seed: int = 0
     outlier_p: float = 0.0
     outlier_mul: float = 1.0
+    # V = (N(0, 1) with outliers + v_offset) * v_mul, for value-range cases
+    v_offset: float = 0.0
+    v_mul: float = 1.0
 
     @property
     def L(self) -> int:
@@ -90,25 +93,27 @@ class Workload:
         g.manual_seed(((self.seed * 1_000_003 + layer) * 131 + stream) * 1_009 + row)
         return g
 
-    def _normal(self, shape, layer, stream, row, outliers, device):
+    def _normal(self, shape, layer, stream, row, outliers, device, value=False):
         g = self._gen(layer, stream, row, device)
         x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
         if outliers and self.outlier_p > 0:
             u = torch.rand(shape, generator=g, device=device)
             x = torch.where(u < self.outlier_p, x * self.outlier_mul, x)
+        if value and (self.v_offset != 0.0 or self.v_mul != 1.0):
+            x = (x + self.v_offset) * self.v_mul
         return x.to(torch.bfloat16)
 
     def context_kv(self, layer: int, row: int, n: int, device="cpu"):
         """bf16 (K, V) [n, Hkv, D] of the first n cached tokens of table row ``row``."""
         shape = (n, self.Hkv, self.D)
         return (self._normal(shape, layer, 1, row, True, device),
-                self._normal(shape, layer, 2, row, True, device))
+                self._normal(shape, layer, 2, row, True, device, value=True))
 
     def step_kv(self, layer: int, device="cpu"):
         """bf16 (K, V) [B, T, Hkv, D] of the tokens each decode row appends."""
         shape = (self.B, self.T, self.Hkv, self.D)
         return (self._normal(shape, layer, 3, 0, True, device),
-                self._normal(shape, layer, 4, 0, True, device))
+                self._normal(shape, layer, 4, 0, True, device, value=True))
 
     def step_q(self, layer: int, device="cpu"):
         """bf16 q [B, T, Hq, D] of the decode rows."""
@@ -118,7 +123,7 @@ class Workload:
         """bf16 (K, V) [Bp, Tc, Hkv, D] of the prefill chunk tokens."""
         shape = (len(self.prefill_rows), self.Tc, self.Hkv, self.D)
         return (self._normal(shape, layer, 6, 0, True, device),
-                self._normal(shape, layer, 7, 0, True, device))
+                self._normal(shape, layer, 7, 0, True, device, value=True))
 
     def chunk_q(self, layer: int, device="cpu"):
         return self._normal((len(self.prefill_rows), self.Tc, self.Hq, self.D), layer, 8, 0, False, device)
