@@ -280,17 +280,17 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
       *reinterpret_cast<uint4*>(f16 + 128 * D + o0) = z ? zero : make_uint4(k2[0], k2[1], k2[2], k2[3]);
       *reinterpret_cast<uint4*>(f16 + 128 * D + o1) = z ? zero : make_uint4(k2[4], k2[5], k2[6], k2[7]);
     }
-    return;
-  }
-  uint4 lo[UPT], hi[UPT];
-  // every raw load of the thread before any store (the stores could alias)
+  } else {
+    uint4 lo[UPT], hi[UPT];
+    // every raw load of the thread before any store (the stores could alias)
 #pragma unroll
-  for (int k = 0; k < UPT; ++k) convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
+    for (int k = 0; k < UPT; ++k) convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
 #pragma unroll
-  for (int k = 0; k < UPT; ++k) {
-    if (rr[k] >= kvalid) lo[k] = hi[k] = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k])) = lo[k];
-    *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k] + 8)) = hi[k];
+    for (int k = 0; k < UPT; ++k) {
+      if (rr[k] >= kvalid) lo[k] = hi[k] = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k])) = lo[k];
+      *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k] + 8)) = hi[k];
+    }
   }
 }
 
