@@ -717,6 +717,9 @@ def run_gpu(args, rank, world):
                                             shared={"k8v4_verify": bench} if w.name == "k8v4_long" else {})
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        one = cpu_baseline_one_thread(args.workload, args.layers, args.context, args.cpu_seconds / 3)
+        if one is not None:
+            line["cpu_baseline"]["value_1_thread"] = one
     return line
 
 
@@ -802,6 +805,22 @@ def cpu_baseline(w, seconds=15.0):
             "sample": f"{n} units of {w.name}, each one (layer, row, KV head) over the row's last "
                       f"min(F, {WINDOW}) keys (its last split-K range, holding the new tokens): "
                       f"encode, decode, float64 attention; {spent:.1f} s of oracle time"}
+
+
+def cpu_baseline_one_thread(name, layers, context, seconds):
+    """The same oracle sample on one host thread: a fresh interpreter whose
+    BLAS and OpenMP pools have one thread (set before NumPy loads); its GB/s,
+    or None when it cannot run."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench; "
+            f"w = bench.make_workload({name!r}, {layers!r}, {context!r}); "
+            f"print(json.dumps(bench.cpu_baseline(w, {seconds!r})))")
+    try:
+        res = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                             timeout=300)
+        return json.loads(res.stdout.strip().splitlines()[-1])["value"] if res.returncode == 0 else None
+    except (subprocess.SubprocessError, ValueError, IndexError, KeyError):
+        return None
 
 
 def run_reference(args, rank, world):
