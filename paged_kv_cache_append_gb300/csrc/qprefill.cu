@@ -164,11 +164,13 @@ __device__ __forceinline__ uint32_t f16_off(int r, int d) {
   return static_cast<uint32_t>((d >> 6) * 8192) + swz<128>(r, (d & 63) * 2);
 }
 
-// 16 dims [16 g, 16 g + 16) of key r: raw codes and scales (shared memory) ->
-// 16 f16 values (two 16-byte chunks).  `shift` is the INT8 key's 2^-e.
+// 16 dims [16 g, 16 g + 16) of key r of an FP8-row or NVFP4-G16 tile: raw
+// codes and scales (shared memory) -> 16 exact f16 values (two 16-byte
+// chunks).  INT8-G64 tiles are converted in convert_tile.
 template <int KIND, int D, int RB>
-__device__ __forceinline__ void convert16(const uint8_t* codes, const uint8_t* scales, int r, int g, float shift,
-                                          uint4& lo, uint4& hi) {
+__device__ __forceinline__ void convert16(const uint8_t* codes, const uint8_t* scales, int r, int g, uint4& lo,
+                                          uint4& hi) {
+  static_assert(KIND == KIND_FP8 || KIND == KIND_NVFP4, "FP8-row and NVFP4-G16 tiles");
   constexpr int SB = scale_row_bytes<KIND>(D);
   if constexpr (KIND == KIND_FP8) {
     const uint4 w = *reinterpret_cast<const uint4*>(codes + raw_off<RB>(r, 16 * g));
@@ -180,22 +182,6 @@ __device__ __forceinline__ void convert16(const uint8_t* codes, const uint8_t* s
                     e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
                     e4m3x2_to_f16x2(static_cast<uint16_t>(w.w & 0xFFFFu)),
                     e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
-  } else if constexpr (KIND == KIND_INT8) {
-    // binary16 code times the binary16 scale s_g 2^-e (exact unless the shift
-    // takes it below binary16's normal range), the product rounded once
-    const uint4 w = *reinterpret_cast<const uint4*>(codes + raw_off<RB>(r, 16 * g));
-    const __half s16 = __float2half_rn(
-        __half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * g) / 64))) * shift);
-    const uint32_t s2 = pack_h2(s16, s16);
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-    uint32_t h[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      h[2 * q] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x1100)), s2);
-      h[2 * q + 1] = hmul2_u32(s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x3322)), s2);
-    }
-    lo = make_uint4(h[0], h[1], h[2], h[3]);
-    hi = make_uint4(h[4], h[5], h[6], h[7]);
   } else {  // NVFP4: 8 bytes of codes times the group's E4M3 scale
     const uint2 w = *reinterpret_cast<const uint2*>(codes + raw_off<RB>(r, 8 * g));
     const uint32_t s16 = e4m3x2_to_f16x2(static_cast<uint16_t>(scales[r * SB + g])) & 0xFFFFu;
@@ -238,27 +224,41 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
   constexpr int UPT = (64 * GPR) / NCT;  // units per thread
   static_assert(UPT * NCT == 64 * GPR && UPT >= 1, "converter units");
   static_assert(!SPLIT || KIND == KIND_INT8, "split tiles are for INT8-G64 keys");
+  // a thread's UPT groups start at a multiple of UPT, so with 16 UPT dividing
+  // 64 they share one INT8-G64 scale group
+  static_assert(KIND != KIND_INT8 || 64 % (16 * UPT) == 0, "one scale group per thread");
   constexpr int SB = scale_row_bytes<KIND>(D);
   const uint8_t* scales = raw + raw_codes;
-  int rr[UPT], gg[UPT];
+  const int r = (ct & 7) + 8 * ((ct >> 3) & 7);  // the thread's key
+  int gg[UPT];
 #pragma unroll
-  for (int k = 0; k < UPT; ++k) {
-    rr[k] = (ct & 7) + 8 * ((ct >> 3) & 7);
-    gg[k] = UPT * (ct >> 6) + (k + ((ct >> 3) & 1)) % UPT;
-  }
-  float shift = 1.f;
-  if constexpr (KIND == KIND_INT8) shift = pow2_neg(int8_row_shift<D>(scales + rr[0] * SB));
-  if constexpr (SPLIT) {
-    // raw codes and scaled scales of every unit first, then convert and store
-    uint4 w[UPT];
-    uint32_t s2[UPT];
+  for (int k = 0; k < UPT; ++k) gg[k] = UPT * (ct >> 6) + (k + ((ct >> 3) & 1)) % UPT;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  if (r >= kvalid) {  // a key at or past the frontier: zeros in every tile
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
-      w[k] = *reinterpret_cast<const uint4*>(raw + raw_off<RB>(rr[k], 16 * gg[k]));
-      const __half s16 = __float2half_rn(
-          __half2float(*reinterpret_cast<const __half*>(scales + rr[k] * SB + 2 * ((16 * gg[k]) / 64))) * shift);
-      s2[k] = pack_h2(s16, s16);
+      const uint32_t o0 = f16_off(r, 16 * gg[k]), o1 = f16_off(r, 16 * gg[k] + 8);
+      *reinterpret_cast<uint4*>(f16 + o0) = zero;
+      *reinterpret_cast<uint4*>(f16 + o1) = zero;
+      if constexpr (SPLIT) {
+        *reinterpret_cast<uint4*>(f16 + 128 * D + o0) = zero;
+        *reinterpret_cast<uint4*>(f16 + 128 * D + o1) = zero;
+      }
     }
+    return;
+  }
+  if constexpr (KIND == KIND_INT8) {
+    // code times the key's shifted binary16 scale s' = s_g 2^-e (once per
+    // thread; exact unless the shift takes it below binary16's normal range),
+    // the product rounded once (k1); SPLIT also stores the remainder k2
+    const float shift = pow2_neg(int8_row_shift<D>(scales + r * SB));
+    const __half s16 =
+        __float2half_rn(__half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * gg[0]) / 64))) * shift);
+    const uint32_t s2 = pack_h2(s16, s16);
+    // every raw load of the thread before any store (the stores could alias)
+    uint4 w[UPT];
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) w[k] = *reinterpret_cast<const uint4*>(raw + raw_off<RB>(r, 16 * gg[k]));
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
       const uint32_t wv[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
@@ -267,29 +267,30 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
       for (int q = 0; q < 4; ++q) {
         const uint32_t c0 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x1100));
         const uint32_t c1 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x3322));
-        k1[2 * q] = hmul2_u32(c0, s2[k]);
-        k1[2 * q + 1] = hmul2_u32(c1, s2[k]);
-        k2[2 * q] = hfma2_u32(c0, s2[k], k1[2 * q] ^ 0x80008000u);
-        k2[2 * q + 1] = hfma2_u32(c1, s2[k], k1[2 * q + 1] ^ 0x80008000u);
+        k1[2 * q] = hmul2_u32(c0, s2);
+        k1[2 * q + 1] = hmul2_u32(c1, s2);
+        if constexpr (SPLIT) {
+          k2[2 * q] = hfma2_u32(c0, s2, k1[2 * q] ^ 0x80008000u);
+          k2[2 * q + 1] = hfma2_u32(c1, s2, k1[2 * q + 1] ^ 0x80008000u);
+        }
       }
-      const bool z = rr[k] >= kvalid;
-      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t o0 = f16_off(rr[k], 16 * gg[k]), o1 = f16_off(rr[k], 16 * gg[k] + 8);
-      *reinterpret_cast<uint4*>(f16 + o0) = z ? zero : make_uint4(k1[0], k1[1], k1[2], k1[3]);
-      *reinterpret_cast<uint4*>(f16 + o1) = z ? zero : make_uint4(k1[4], k1[5], k1[6], k1[7]);
-      *reinterpret_cast<uint4*>(f16 + 128 * D + o0) = z ? zero : make_uint4(k2[0], k2[1], k2[2], k2[3]);
-      *reinterpret_cast<uint4*>(f16 + 128 * D + o1) = z ? zero : make_uint4(k2[4], k2[5], k2[6], k2[7]);
+      const uint32_t o0 = f16_off(r, 16 * gg[k]), o1 = f16_off(r, 16 * gg[k] + 8);
+      *reinterpret_cast<uint4*>(f16 + o0) = make_uint4(k1[0], k1[1], k1[2], k1[3]);
+      *reinterpret_cast<uint4*>(f16 + o1) = make_uint4(k1[4], k1[5], k1[6], k1[7]);
+      if constexpr (SPLIT) {
+        *reinterpret_cast<uint4*>(f16 + 128 * D + o0) = make_uint4(k2[0], k2[1], k2[2], k2[3]);
+        *reinterpret_cast<uint4*>(f16 + 128 * D + o1) = make_uint4(k2[4], k2[5], k2[6], k2[7]);
+      }
     }
   } else {
     uint4 lo[UPT], hi[UPT];
     // every raw load of the thread before any store (the stores could alias)
 #pragma unroll
-    for (int k = 0; k < UPT; ++k) convert16<KIND, D, RB>(raw, scales, rr[k], gg[k], shift, lo[k], hi[k]);
+    for (int k = 0; k < UPT; ++k) convert16<KIND, D, RB>(raw, scales, r, gg[k], lo[k], hi[k]);
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
-      if (rr[k] >= kvalid) lo[k] = hi[k] = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k])) = lo[k];
-      *reinterpret_cast<uint4*>(f16 + f16_off(rr[k], 16 * gg[k] + 8)) = hi[k];
+      *reinterpret_cast<uint4*>(f16 + f16_off(r, 16 * gg[k])) = lo[k];
+      *reinterpret_cast<uint4*>(f16 + f16_off(r, 16 * gg[k] + 8)) = hi[k];
     }
   }
 }
