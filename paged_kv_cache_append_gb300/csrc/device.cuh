@@ -262,6 +262,18 @@ __device__ __forceinline__ uint32_t s8pair_to_f16x2(uint32_t w_pair_in_bytes_0_2
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// The same from a word whose sign bits were flipped already (w ^ 0x80808080,
+// once per four codes): the pair (b_2k, b_2k+1) of the word -> f16x2, built
+// by one byte permute against the 0x64 exponent bytes.
+template <int K>
+__device__ __forceinline__ uint32_t s8pair_flipped_to_f16x2(uint32_t w_flipped) {
+  static_assert(K == 0 || K == 1, "pair 0 (bytes 0, 1) or 1 (bytes 2, 3)");
+  const uint32_t x = __byte_perm(w_flipped, 0x64646464u, K == 0 ? 0x4140 : 0x4342);
+  const __half2 h = *reinterpret_cast<const __half2*>(&x);
+  const __half2 r = __hsub2(h, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&r);

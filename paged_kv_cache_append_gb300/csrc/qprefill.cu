@@ -51,9 +51,9 @@
 // binary16's normal range, where the element's error stays under 2^-32 of the
 // key's largest element):
 //   * keys are exact: each K tile is held as two f16 tiles k1 = f16(c s') and
-//     k2 = c s' - k1 (an f16 value, see convert_tile), and S accumulates
-//     Q k1^T + Q k2^T, so the scores are those of the dequantized keys up to
-//     the fp32 accumulation;
+//     k2' = k1 - c s' (an f16 value, see convert_tile), and S accumulates
+//     Q k1^T - Q k2'^T (the second MMA negates its B operand), so the scores
+//     are those of the dequantized keys up to the fp32 accumulation;
 //   * values are rounded once, c s' to f16 (relative error <= 2^-11 per
 //     element, as the f16 softmax weights themselves).
 #include <cmath>
@@ -214,10 +214,11 @@ __device__ __forceinline__ float key_factor(const uint8_t* scales, int r) {
 // `kvalid` become zeros.
 //
 // SPLIT (INT8-G64 only): the tile is written twice, as k1 = f16(c s') and, at
-// f16 + 64 D 2, as k2 = f16(c s' - k1), with s' = s_g 2^-e the binary16
-// scale.  c s' is a multiple of 2^-24 with at most 7 + 11 significant bits, so
-// the remainder c s' - k1 (at most 7 bits, the same multiple) is an f16 value
-// and k1 + k2 = c s' exactly: one f16 FMA per pair gives it.
+// f16 + 64 D 2, as the negated remainder k2' = k1 - c s', with s' = s_g 2^-e
+// the binary16 scale.  c s' is a multiple of 2^-24 with at most 7 + 11
+// significant bits, so the remainder (at most 7 bits, the same multiple) is an
+// f16 value and k1 - k2' = c s' exactly: one f16 FMA per pair, fma(c, -s', k1),
+// gives it, and the MMA that reads k2' negates its B operand.
 template <int KIND, int D, int RB, int NCT, bool SPLIT = false>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, uint8_t* f16, int ct, int kvalid) {
   constexpr int GPR = D / 16;            // 16-dim groups per key
@@ -254,24 +255,25 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, int raw_codes, 
     const float shift = pow2_neg(int8_row_shift<D>(scales + r * SB));
     const __half s16 =
         __float2half_rn(__half2float(*reinterpret_cast<const __half*>(scales + r * SB + 2 * ((16 * gg[0]) / 64))) * shift);
-    const uint32_t s2 = pack_h2(s16, s16);
+    const uint32_t s2 = pack_h2(s16, s16), s2n = s2 ^ 0x80008000u;  // s', -s'
     // every raw load of the thread before any store (the stores could alias)
     uint4 w[UPT];
 #pragma unroll
     for (int k = 0; k < UPT; ++k) w[k] = *reinterpret_cast<const uint4*>(raw + raw_off<RB>(r, 16 * gg[k]));
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
-      const uint32_t wv[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+      const uint32_t wv[4] = {w[k].x ^ 0x80808080u, w[k].y ^ 0x80808080u, w[k].z ^ 0x80808080u,
+                              w[k].w ^ 0x80808080u};
       uint32_t k1[8], k2[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t c0 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x1100));
-        const uint32_t c1 = s8pair_to_f16x2(__byte_perm(wv[q], 0, 0x3322));
+        const uint32_t c0 = s8pair_flipped_to_f16x2<0>(wv[q]);
+        const uint32_t c1 = s8pair_flipped_to_f16x2<1>(wv[q]);
         k1[2 * q] = hmul2_u32(c0, s2);
         k1[2 * q + 1] = hmul2_u32(c1, s2);
         if constexpr (SPLIT) {
-          k2[2 * q] = hfma2_u32(c0, s2, k1[2 * q] ^ 0x80008000u);
-          k2[2 * q + 1] = hfma2_u32(c1, s2, k1[2 * q + 1] ^ 0x80008000u);
+          k2[2 * q] = hfma2_u32(c0, s2n, k1[2 * q]);
+          k2[2 * q + 1] = hfma2_u32(c1, s2n, k1[2 * q + 1]);
         }
       }
       const uint32_t o0 = f16_off(r, 16 * gg[k]), o1 = f16_off(r, 16 * gg[k] + 8);
@@ -526,15 +528,16 @@ __global__ void __launch_bounds__((QCfg<KK, KV, D>::THREADS), 1)
             ok = mbar_wait_bounded(&k_full[ks], (j / NK) & 1, a.status) && !*s_abort;
             if (!ok) break;
             tc::fence_after();
-            // INT8-G64: the two f16 tiles of the split keys accumulate into S
+            // INT8-G64: S = Q k1^T - Q k2'^T from the two f16 tiles of the
+            // split keys (the second MMA negates its B operand)
 #pragma unroll
             for (int part = 0; part < (Cfg::K_SPLIT ? 2 : 1); ++part) {
               const uint64_t kd = tc::smem_desc(smem_u32(sK + ks * Cfg::K_STAGE + part * Cfg::F16), 16, 1024);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk)
                 tc::mma_ts(tmem + Cfg::COL_S + 64 * sb, tmem + Cfg::COL_Q + kk * 8,
-                           kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), Cfg::ID_S,
-                           part > 0 || kk > 0);
+                           kd + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+                           part > 0 ? tc::idesc_negate_b(Cfg::ID_S) : Cfg::ID_S, part > 0 || kk > 0);
             }
             tc::commit(&s_full[sb]);
             tc::commit(&k_empty[ks]);

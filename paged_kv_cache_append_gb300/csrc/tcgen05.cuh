@@ -160,6 +160,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same descriptor with the B operand negated (bit 14).
+__host__ __device__ constexpr uint32_t idesc_negate_b(uint32_t idesc) { return idesc | (1u << 14); }
+
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0
 // in both fields) and an fp32 accumulator, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
