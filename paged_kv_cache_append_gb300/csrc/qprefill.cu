@@ -11,7 +11,7 @@
 //   warp 4      TMA producer: the raw code tile of each page (the pool's own
 //               tensor maps, 64 rows x min(row bytes, 128) boxes) and its
 //               scale tile (bulk copy) into a raw K ring and a raw V ring;
-//   warps 6-9   converters: each page's codes become an f16 tile in the
+//   warps 6-13  converters: each page's codes become an f16 tile in the
 //               layout the MMAs read (rows = keys, 128-byte rows of 64 dims,
 //               128-byte swizzle), K one page ahead of V; with K they
 //               store each key's fp32 factors (K: score factor times
@@ -105,9 +105,10 @@ constexpr float kLazyThr = 8.f;
 
 template <int KK, int KV, int D>
 struct QCfg {
-  // converter warps (6 .. 5 + NCONV): 8 where K and V are both converted, 4
-  // where only V is (the raw FP8 keys go to the tensor cores)
-  static constexpr int NCONV = (KK == KIND_FP8 && D >= 128) ? 4 : 8;
+  // converter warps (6 .. 5 + NCONV), 8 for every profile: the conversion
+  // work sets the pace where only V is converted (raw FP8 keys go to the
+  // tensor cores) as well as where both are
+  static constexpr int NCONV = 8;
   static constexpr int THREADS = 192 + 32 * NCONV;  // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int KCB = code_row_bytes<KK>(D), VCB = code_row_bytes<KV>(D);
   static constexpr int KSB = scale_row_bytes<KK>(D), VSB = scale_row_bytes<KV>(D);
