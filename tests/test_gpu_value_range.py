@@ -1,7 +1,8 @@
 """GPU parity when V is far from unit scale, through the C ABI.
 
 V = (N(0, 1) with 1% outliers x20 + 0.5) * v_mul for v_mul from 2^-14 to
-2^17, with a sharp softmax (scale 4 / sqrt(D)).  The codec rules fix what the
+2^22 (where the outliers saturate the INT8-G64 and FP8-row binary16 scales at
+65504), with a sharp softmax (scale 4 / sqrt(D)).  The codec rules fix what the
 pages hold at every magnitude (binary16 scales go subnormal for small V and
 saturate at 65504 for large INT8-G64 V; NVFP4 flushes to zero below its E4M3
 range and saturates above it); the attention over those dequantized values
@@ -36,7 +37,7 @@ from tests.scenario import Scenario, compare_attention
 pytestmark = pytest.mark.gpu
 
 PROFILES = ["bf16", "int8_g64", "fp8_row", "nvfp4_g16", "k8v4"]
-V_MULS = [2.0 ** -14, 2.0 ** -8, 2.0 ** 10, 2.0 ** 17]
+V_MULS = [2.0 ** -14, 2.0 ** -8, 2.0 ** 10, 2.0 ** 17, 2.0 ** 22]
 
 
 def _workload(profile, D, G, T, seed, v_mul, contexts, S, prefill=None):
