@@ -797,7 +797,10 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         if constexpr (KV == KIND_NVFP4) {
           const int colb = d0 / 2;  // 16 code bytes, two scale bytes
           const uint4 w = *reinterpret_cast<const uint4*>(vtile + (colb / RB) * (64 * RB) + swz<RB>(vkey, colb % RB));
-          const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vs_tile + vkey * Cfg::VSB + d0 / 16));
+          // a key past the frontier gets zero scales: its E2M1 codes are
+          // finite, so every product is 0 (stale scale bytes never enter)
+          const uint32_t s2 =
+              vlive ? e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(vs_tile + vkey * Cfg::VSB + d0 / 16)) : 0u;
           const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {  // 16 dims, one scale group
@@ -811,16 +814,16 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
               hv[4 * q + 3] = hmul2_u32(e2m1x2_byte_to_f16x2<3>(wv[2 * sub + q]), sq);
             }
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const uint4 v = vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
-                                    : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(blk + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) = v;
-            }
+            for (int k = 0; k < 2; ++k)
+              *reinterpret_cast<uint4*>(blk + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) =
+                  make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
           }
         } else {  // INT8 / FP8: 16 code bytes per 16 dims
           const uint16_t* sp = reinterpret_cast<const uint16_t*>(vs_tile);
           const uint32_t s1 = KV == KIND_INT8 ? sp[vkey * (Cfg::VSB / 2) + d0 / 64] : sp[vkey];
-          const uint32_t s2 = hmul2_u32(s1 | (s1 << 16), lift2);
+          // INT8 codes are finite, so a zero scale zeroes a key past the
+          // frontier; FP8 codes may encode NaN there and are selected away
+          const uint32_t s2 = KV == KIND_INT8 && !vlive ? 0u : hmul2_u32(s1 | (s1 << 16), lift2);
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {
             const int dd = d0 + 16 * sub;
@@ -839,8 +842,8 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const uint4 v = vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
-                                    : make_uint4(0u, 0u, 0u, 0u);
+              const uint4 v = KV == KIND_INT8 || vlive ? make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3])
+                                                       : make_uint4(0u, 0u, 0u, 0u);
               *reinterpret_cast<uint4*>(blk + swz<128>(kr, 64 * dh + 32 * sub + 16 * k)) = v;
             }
           }
@@ -906,6 +909,10 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
           }
           slo = hmul2_u32(slo, lift2);
           shi = hmul2_u32(shi, lift2);
+          if constexpr (KV == KIND_INT8) {  // finite codes: zero scales zero the keys past the frontier
+            slo &= mlo;
+            shi &= mhi;
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if constexpr (KV == KIND_INT8) {
@@ -921,8 +928,10 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
         }
 #pragma unroll
         for (int mg = 0; mg < 2; ++mg) {
-          const uint32_t A[4] = {pair_lo[2 * mg] & mlo, pair_lo[2 * mg + 1] & mlo,
-                                 pair_hi[2 * mg] & mhi, pair_hi[2 * mg + 1] & mhi};
+          // keys past the frontier are zero (INT8: through their scales)
+          const uint32_t ml = KV == KIND_INT8 ? 0xFFFFFFFFu : mlo, mh = KV == KIND_INT8 ? 0xFFFFFFFFu : mhi;
+          const uint32_t A[4] = {pair_lo[2 * mg] & ml, pair_lo[2 * mg + 1] & ml,
+                                 pair_hi[2 * mg] & mh, pair_hi[2 * mg + 1] & mh};
 #pragma unroll
           for (int j = 0; j < NQT; ++j) mma16816<false>(o[2 * p + mg][j], A, pb[0][j][0], pb[0][j][1]);
         }
