@@ -694,26 +694,53 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     const int kg0 = key0 + kr0, kg1 = key0 + kr1;
     float alpha[NQT][2];
     bool rescale = false;
+    // Lazy rescale: a row's reference maximum moves only when one of its
+    // scores passes it by more than 2^8 (log2 units), so p <= 2^8 (exact in
+    // the f16 / bf16 operands, harmless to the fp32 accumulators); a warp
+    // vote on the thread-local maxima skips the cross-lane reduction of every
+    // other page.
+    float vloc[NQT][2];
+    bool need = false;
 #pragma unroll
     for (int j = 0; j < NQT; ++j) {
       S[j][0] = kg0 <= lim[j][0] ? S[j][0] * sc : -INFINITY;
       S[j][1] = kg0 <= lim[j][1] ? S[j][1] * sc : -INFINITY;
       S[j][2] = kg1 <= lim[j][0] ? S[j][2] * sc : -INFINITY;
       S[j][3] = kg1 <= lim[j][1] ? S[j][3] * sc : -INFINITY;
-      float v[2] = {fmaxf(S[j][0], S[j][2]), fmaxf(S[j][1], S[j][3])};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) v[u] = fmaxf(v[u], __shfl_xor_sync(0xffffffffu, v[u], off));
-        const float mx2 = fmaxf(m_run[j][u], v[u]);
-        const float mu = mx2 == -INFINITY ? 0.f : mx2;
-        alpha[j][u] = ex2(m_run[j][u] - mu);
-        rescale |= (mx2 != m_run[j][u]);
-        m_run[j][u] = mx2;
-        S[j][u] = ex2(S[j][u] - mu);
-        S[j][2 + u] = ex2(S[j][2 + u] - mu);
-        l_part[j][u] = l_part[j][u] * alpha[j][u] + S[j][u] + S[j][2 + u];
+        vloc[j][u] = fmaxf(S[j][u], S[j][2 + u]);
+        need |= vloc[j][u] > m_run[j][u] + 8.f;  // also a row leaving -inf
       }
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int j = 0; j < NQT; ++j)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float v = vloc[j][u];
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          const float mx2 = fmaxf(m_run[j][u], v);
+          const float mu = mx2 == -INFINITY ? 0.f : mx2;
+          alpha[j][u] = ex2(m_run[j][u] - mu);
+          rescale |= (mx2 != m_run[j][u]);
+          m_run[j][u] = mx2;
+          S[j][u] = ex2(S[j][u] - mu);
+          S[j][2 + u] = ex2(S[j][2 + u] - mu);
+          l_part[j][u] = l_part[j][u] * alpha[j][u] + S[j][u] + S[j][2 + u];
+        }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NQT; ++j)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float mu = m_run[j][u] == -INFINITY ? 0.f : m_run[j][u];
+          alpha[j][u] = 1.f;
+          S[j][u] = ex2(S[j][u] - mu);
+          S[j][2 + u] = ex2(S[j][2 + u] - mu);
+          l_part[j][u] += S[j][u] + S[j][2 + u];
+        }
     }
     if (__any_sync(0xffffffffu, rescale) || knew != k_run) {
       const float kf = pow2i(knew - k_run);
