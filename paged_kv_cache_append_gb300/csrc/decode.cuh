@@ -27,7 +27,8 @@
 //       two halves are added through shared memory (same order in both
 //       warps).  INT8-G64 group scales and FP8 row scales multiply fp32
 //       partial sums; NVFP4 scales multiply the f16 operand (exact product).
-//  softmax: base-2, running max per query row over the pair's keys.
+//  softmax: base-2, per query row over the pair's keys, with a lazy reference
+//       maximum that moves only when a score passes it by more than 2^8.
 //  PV:  O^T (the warp's dims x R) += V^T P^T with P^T taken straight from the
 //       S registers by movmatrix, V^T built in registers from the V tile
 //       (ldmatrix.trans for bf16; byte gathers for 8-bit and 4-bit codes), V
