@@ -495,7 +495,9 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   };
 
   // ---- running state -----------------------------------------------------------
-  float m_run[NQT][2], l_part[NQT][2];
+  // nm: minus the row's reference maximum (0 before the row's first key),
+  // folded into the score scaling as one FFMA per score
+  float nm[NQT][2], l_part[NQT][2];
   float o[MTW][NQT][4];
   // INT8-G64 / FP8-row V: the values are f16 products code * (s 2^k_run), with
   // k_run <= 0 the lift of the largest value scale this warp has read
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
   int k_run = 0;
 #pragma unroll
   for (int j = 0; j < NQT; ++j) {
-    m_run[j][0] = m_run[j][1] = -INFINITY;
+    nm[j][0] = nm[j][1] = 0.f;
     l_part[j][0] = l_part[j][1] = 0.f;
   }
 #pragma unroll
@@ -699,19 +701,22 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
     // scores passes it by more than 2^8 (log2 units), so p <= 2^8 (exact in
     // the f16 / bf16 operands, harmless to the fp32 accumulators); a warp
     // vote on the thread-local maxima skips the cross-lane reduction of every
-    // other page.
+    // other page.  S becomes t = s - reference.  The first page always takes
+    // the exact maximum: a row's visible keys are a prefix of the keys, so a
+    // row with no visible key on the warp's first page has none later.
+    const bool first = (i == 0);
     float vloc[NQT][2];
-    bool need = false;
+    bool need = first;
 #pragma unroll
     for (int j = 0; j < NQT; ++j) {
-      S[j][0] = kg0 <= lim[j][0] ? S[j][0] * sc : -INFINITY;
-      S[j][1] = kg0 <= lim[j][1] ? S[j][1] * sc : -INFINITY;
-      S[j][2] = kg1 <= lim[j][0] ? S[j][2] * sc : -INFINITY;
-      S[j][3] = kg1 <= lim[j][1] ? S[j][3] * sc : -INFINITY;
+      S[j][0] = kg0 <= lim[j][0] ? fmaf(S[j][0], sc, nm[j][0]) : -INFINITY;
+      S[j][1] = kg0 <= lim[j][1] ? fmaf(S[j][1], sc, nm[j][1]) : -INFINITY;
+      S[j][2] = kg1 <= lim[j][0] ? fmaf(S[j][2], sc, nm[j][0]) : -INFINITY;
+      S[j][3] = kg1 <= lim[j][1] ? fmaf(S[j][3], sc, nm[j][1]) : -INFINITY;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         vloc[j][u] = fmaxf(S[j][u], S[j][2 + u]);
-        need |= vloc[j][u] > m_run[j][u] + 8.f;  // also a row leaving -inf
+        need |= vloc[j][u] > 8.f;
       }
     }
     if (__any_sync(0xffffffffu, need)) {
@@ -722,13 +727,14 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
           float v = vloc[j][u];
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          const float mx2 = fmaxf(m_run[j][u], v);
-          const float mu = mx2 == -INFINITY ? 0.f : mx2;
-          alpha[j][u] = ex2(m_run[j][u] - mu);
-          rescale |= (mx2 != m_run[j][u]);
-          m_run[j][u] = mx2;
-          S[j][u] = ex2(S[j][u] - mu);
-          S[j][2 + u] = ex2(S[j][2 + u] - mu);
+          // first page: the reference becomes the row's maximum (l and O are
+          // still 0); later: it moves up by the excess, if any
+          const float shift = first ? (v == -INFINITY ? 0.f : v) : fmaxf(v, 0.f);
+          alpha[j][u] = first ? 0.f : ex2(-shift);
+          rescale |= shift > 0.f;
+          nm[j][u] -= shift;
+          S[j][u] = ex2(S[j][u] - shift);
+          S[j][2 + u] = ex2(S[j][2 + u] - shift);
           l_part[j][u] = l_part[j][u] * alpha[j][u] + S[j][u] + S[j][2 + u];
         }
     } else {
@@ -736,10 +742,9 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       for (int j = 0; j < NQT; ++j)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float mu = m_run[j][u] == -INFINITY ? 0.f : m_run[j][u];
           alpha[j][u] = 1.f;
-          S[j][u] = ex2(S[j][u] - mu);
-          S[j][2 + u] = ex2(S[j][2 + u] - mu);
+          S[j][u] = ex2(S[j][u]);
+          S[j][2 + u] = ex2(S[j][2 + u]);
           l_part[j][u] += S[j][u] + S[j][2 + u];
         }
     }
@@ -971,6 +976,9 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
 
   // ---- combine the four pairs (fixed order), write partials or the output -----------
   // Both warps of a pair hold the same (m, l); each holds O for its own dims.
+  // m is the reference maximum, -inf for a row that saw no key (l = 0; a row
+  // that saw one has l >= 1: its maximum key had p = 1 when it was taken).
+  float m_run[NQT][2];
 #pragma unroll
   for (int j = 0; j < NQT; ++j)
 #pragma unroll
@@ -979,6 +987,7 @@ __global__ void __launch_bounds__((DecodeCfg<KK, KV, D, NQT>::THREADS), (DecodeC
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 16);
+      m_run[j][u] = v > 0.f ? -nm[j][u] : -INFINITY;
       if (r == 0 && half == 0) {
         red_m[pair * R + 8 * j + 2 * c + u] = m_run[j][u];
         red_l[pair * R + 8 * j + 2 * c + u] = v;
